@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of one full verify step on synthetic data.
+
+A step is one pass of the whole hot path over one batch: tree-verify
+attention with chunk salience for every layer (scores summed over layers),
+top-k chunk selection plus window gathered into the compact cache, and tree
+acceptance.  Default workload: Llama-3.1-8B KV shapes at 128K context with a
+64-node tree, 32 layers, greedy acceptance over a 128,256-token vocabulary.
+
+Prints one JSON line (rank 0).  `value` is microseconds per verify step per
+layer (step time / layers; with N replicas, the whole job's step time per
+layer-step: ms / (layers * N)), so lower is better.  Inputs stay resident in
+HBM; every layer's K/V cache is a distinct 537 MB tensor, larger than L2.
+
+--impl reference times the float64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload each step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("µs/verify-step/layer and KV GB/s (% HBM peak) at 128K ctx, "
+          "64-node tree")
+UNIT = "us/verify-step/layer"
+DEFAULT_WORKLOAD = "llama8b-128k-32l"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kv_bytes(wl, st):
+    return sum((L + T) for L, T in zip(st.ctx_lens, st.tree_sizes)) * \
+        wl.num_kv_heads * wl.head_dim * 2 * 2
+
+
+def _q_bytes(wl, st):
+    return st.n_nodes * wl.num_q_heads * wl.head_dim * 2
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ds_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+
+def oracle_sample(wl, st, layer_inputs, accept_inp, heads_sampled: int):
+    """Times the float64 oracle on a bounded sample of one step: one layer's
+    verify attention restricted to `heads_sampled` kv heads (with their query
+    heads), the top-k gather, and acceptance.  Returns (seconds per full step
+    per layer, description)."""
+    import numpy as np
+    from oracle import ref
+    q, k, v = layer_inputs
+    G = wl.num_q_heads // wl.num_kv_heads
+    f64 = lambda t: t.detach().cpu().to(__import__("torch").float64).numpy()
+    qs = f64(q[:, :G * heads_sampled])
+    ks = f64(k[:, :, :heads_sampled])
+    vs = f64(v[:, :, :heads_sampled])
+    t0 = time.perf_counter()
+    _, scores, _ = ref.verify_attention(qs, ks, vs, st.page_table.numpy(),
+                                        st.ctx_lens, st.tree_offsets,
+                                        st.parents, wl.page_size,
+                                        wl.chunk_size)
+    t_verify = (time.perf_counter() - t0) * wl.num_kv_heads / heads_sampled
+    kb = k[:, :, :1].contiguous().view(__import__("torch").int16).numpy() \
+        .view(np.uint16)
+    t0 = time.perf_counter()
+    cap = wl.top_k * wl.chunk_size + wl.window
+    ref.gather_compact(kb, kb, st.page_table.numpy(), st.ctx_lens, scores,
+                       wl.page_size, wl.chunk_size, wl.top_k, wl.window, cap)
+    # gather moved one kv head of K twice; scale to all heads of K and V
+    t_gather = (time.perf_counter() - t0) * wl.num_kv_heads
+    t0 = time.perf_counter()
+    tl = accept_inp.target_logits.cpu().numpy()
+    toks = accept_inp.draft_tokens.cpu().numpy()
+    if wl.accept == "reject":
+        ref.rejection_accept(tl, accept_inp.draft_logits.cpu().numpy(), toks,
+                             st.parents, st.tree_offsets,
+                             accept_inp.uniforms.cpu().numpy())
+    else:
+        ref.greedy_accept(tl, toks, st.parents, st.tree_offsets)
+    t_accept = time.perf_counter() - t0
+    per_layer = (t_verify * wl.layers + t_gather + t_accept) / wl.layers
+    desc = (f"1 layer of verify attention on {heads_sampled}/{wl.num_kv_heads} "
+            f"kv heads (scaled x{wl.num_kv_heads // heads_sampled}, then x"
+            f"{wl.layers} layers), top-k gather of 1 kv head of K (scaled), "
+            f"full acceptance; divided by {wl.layers} layers")
+    return per_layer, desc
+
+
+def cpu_inputs(wl):
+    import torch
+    from long_context_speculative_ds_gb300 import synth
+    st = synth.make_structure(wl)
+    q, k, v = synth.make_layer(st, 0, device="cpu")
+    mode = "reject" if wl.accept == "reject" else "greedy"
+    acc = synth.make_accept_inputs(st, mode)
+    return st, (q, k, v), acc
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    st, layer, acc = cpu_inputs(wl)
+    for _ in range(args.warmup):
+        oracle_sample(wl, st, layer, acc, 1)
+    per = []
+    desc = ""
+    for _ in range(args.steps):
+        s, desc = oracle_sample(wl, st, layer, acc, 1)
+        per.append(s)
+    us = statistics.mean(per) * 1e6
+    kvb = _kv_bytes(wl, st)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us * wl.layers / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, st),
+        "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 3),
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, st):
+    return {"workload": wl.name, "batch": wl.batch,
+            "ctx_lens": st.ctx_lens if wl.batch <= 8 else "ragged",
+            "tree_nodes": st.tree_sizes, "layers": wl.layers,
+            "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+            "head_dim": wl.head_dim, "page_size": wl.page_size,
+            "chunk_size": wl.chunk_size, "top_k": wl.top_k,
+            "window": wl.window, "vocab": wl.vocab, "accept": wl.accept,
+            "l2": "inputs larger than L2: every layer has its own "
+                  f"{_kv_bytes(wl, st) / 1e6:.0f} MB K/V cache"}
+
+
+def _traffic_for(src_path: str):
+    """DRAM bytes per launch of the split pass from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "verify_split_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    sha = hashlib.sha256(open(src_path, "rb").read()).hexdigest()
+    if d.get("source_sha256") != sha:
+        return None
+    return d.get("dram_bytes_per_launch_full_size")
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from long_context_speculative_ds_gb300 import binding, synth
+    from long_context_speculative_ds_gb300 import build as bld
+    from long_context_speculative_ds_gb300.step import StepInputs, VerifyStep
+
+    if not bld.up_to_date():
+        if world > 1:
+            raise RuntimeError("library not built; run __graft_entry__.build()")
+        bld.build()
+    binding.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    st = synth.make_structure(wl)
+    qs, ks, vs = [], [], []
+    for l in range(wl.layers):
+        q, k, v = synth.make_layer(st, l, device=dev)
+        qs.append(q); ks.append(k); vs.append(v)
+    sk, sv = synth.make_source_cache(st, device=dev)
+    mode = "reject" if wl.accept == "reject" else "greedy"
+    acc = synth.make_accept_inputs(st, mode, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    inp = StepInputs(page_table=st.page_table.to(dev),
+                     ctx_lens=torch.tensor(st.ctx_lens, **i32),
+                     tree_offsets=torch.tensor(st.tree_offsets, **i32),
+                     parents=torch.tensor(st.parents, **i32),
+                     q=qs, k_cache=ks, v_cache=vs, src_k=sk, src_v=sv,
+                     target_logits=acc.target_logits,
+                     draft_logits=acc.draft_logits,
+                     draft_tokens=acc.draft_tokens, uniforms=acc.uniforms)
+    step = VerifyStep(inp, chunk_size=wl.chunk_size, top_k=wl.top_k,
+                      window=wl.window, accept_mode=mode)
+    # per-layer events around the split-pass kernel
+    n_ev = args.steps * wl.layers
+    evs = [(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    prof_args = []
+    for i in range(n_ev):
+        l = i % wl.layers
+        prof_args.append(binding.verify_args(
+            inp.q[l], inp.k_cache[l], inp.v_cache[l], inp.page_table,
+            inp.ctx_lens, inp.tree_offsets, inp.parents,
+            chunk_size=wl.chunk_size, out=step.out[l],
+            chunk_scores=step.scores, workspace=step.ws_verify,
+            accumulate=l > 0, prof_events=evs[i]))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+
+    sampler = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(args.steps):
+        for l in range(wl.layers):
+            binding.ds_verify_attn(prof_args[s * wl.layers + l])
+        step.gather()
+        step.accept()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: pinned host inputs in, results out, every step
+    host = StepInputs(
+        page_table=inp.page_table.cpu().pin_memory(),
+        ctx_lens=inp.ctx_lens.cpu().pin_memory(),
+        tree_offsets=inp.tree_offsets.cpu().pin_memory(),
+        parents=inp.parents.cpu().pin_memory(),
+        q=[x.cpu().pin_memory() for x in inp.q], k_cache=[], v_cache=[],
+        src_k=None, src_v=None,
+        target_logits=inp.target_logits.cpu().pin_memory(),
+        draft_logits=None if inp.draft_logits is None else inp.draft_logits.cpu().pin_memory(),
+        draft_tokens=inp.draft_tokens.cpu().pin_memory(),
+        uniforms=None if inp.uniforms is None else inp.uniforms.cpu().pin_memory())
+    host_out = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory()
+                for n in ("out_path", "out_n", "out_bonus", "out_chunk_ids",
+                          "out_len")}
+    h2d = d2h = 0
+    for _ in range(max(1, min(args.warmup, 2))):
+        step.upload(host); step.run(); step.download(host_out)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        h2d = step.upload(host)
+        step.run()
+        d2h = step.download(host_out)
+        torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert step.device_status() == 0
+
+    if rank != 0:
+        return
+    kvb = _kv_bytes(wl, st)
+    peak, peak_kind = _peaks()
+    us = ms * 1e3 / (wl.layers * world)
+    kv_gbs = kvb * wl.layers * world / (ms * 1e-3) / 1e9
+    alg_bytes = kvb + _q_bytes(wl, st)
+    achieved = alg_bytes / (split_ms * 1e-3) / 1e9
+    src = os.path.join(ROOT, "long_context_speculative_ds_gb300", "csrc",
+                       "verify_attn.cu")
+    line = {
+        "metric": METRIC, "value": round(us, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(wl, st),
+        "kv_gbs": round(kv_gbs, 1),
+        "hbm_frac": round(kv_gbs / peak, 4),
+        "roofline": {"kernel": "verify split pass", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "split_pass_us": round(split_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "traffic": _traffic_for(src)},
+        "e2e": {"value": round(e2e_ms * 1e3 / (wl.layers * world), 3),
+                "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "committed and tree K/V stay resident (model state);"
+                        " per-step Q, tree, page table, logits, uniforms in,"
+                        " path/bonus/chunk ids out"},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cst, layer, cacc = cpu_inputs(wl)
+        t, desc = oracle_sample(wl, cst, layer, cacc, 1)
+        line["cpu_baseline"] = {"value": round(t * 1e6, 1), "unit": UNIT,
+                                "cores": len(os.sched_getaffinity(0)),
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from long_context_speculative_ds_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

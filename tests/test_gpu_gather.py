@@ -1,0 +1,114 @@
+"""GPU parity of ds_chunk_topk_gather, through the C ABI.
+
+The chosen chunk ids must equal the oracle's selection rule applied to the
+same scores, bit for bit; the compact K/V bytes, positions and lengths must
+equal the oracle's gather.  At full size the selection is also compared with
+the selection made from float64 oracle scores: any difference must be a
+near-tie (|s_k - s_(k+1)| <= 1e-3 s_k), and every planted salient chunk must
+be chosen.
+"""
+import numpy as np
+import pytest
+import torch
+
+from long_context_speculative_ds_gb300 import synth
+from oracle import ref
+import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_gather(wl, st, inp, step, scores_np, layout):
+    cap = step.capacity
+    exp = ref.gather_compact(H.bits(inp.src_k), H.bits(inp.src_v),
+                             st.page_table.numpy(), st.ctx_lens, scores_np,
+                             wl.page_size, wl.chunk_size, wl.top_k, wl.window,
+                             cap, layout=layout)
+    ids = step.out_chunk_ids.cpu().numpy()[:, :wl.top_k]
+    np.testing.assert_array_equal(ids, exp["chunk_ids"])
+    np.testing.assert_array_equal(step.out_len.cpu().numpy(), exp["out_len"])
+    np.testing.assert_array_equal(step.out_positions.cpu().numpy(),
+                                  exp["positions"])
+    ok, ov = H.bits(step.out_k), H.bits(step.out_v)
+    for b in range(wl.batch):
+        n = exp["out_len"][b]
+        np.testing.assert_array_equal(ok[b, :n], exp["out_k"][b, :n])
+        np.testing.assert_array_equal(ov[b, :n], exp["out_v"][b, :n])
+
+
+def _set_scores(step, scores_np):
+    step.scores.copy_(torch.from_numpy(scores_np.astype(np.float32)))
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_select_and_gather_with_ties(layout, seed):
+    wl = synth.tiny_workload(batch=4, chunk_size=32, top_k=5, window=70,
+                             head_dim=128, num_q_heads=8, num_kv_heads=4)
+    st, inp, mode = H.build_case(wl, layout=layout, seed=seed,
+                                 ctx_lens=(2000, 500, 40, 0), tree_sizes=(3, 2, 2, 1))
+    step = H.make_step(wl, inp, mode, layout)
+    rng = np.random.default_rng(seed)
+    scores = (rng.integers(0, 6, size=step.scores.shape) * 0.5).astype(np.float32)
+    _set_scores(step, scores)
+    step.gather()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    _check_gather(wl, st, inp, step, scores.astype(np.float64), layout)
+
+
+def test_topk_larger_than_candidates_and_zero_k():
+    wl = synth.tiny_workload(batch=2, chunk_size=16, top_k=50, window=16)
+    st, inp, mode = H.build_case(wl, ctx_lens=(300, 33), tree_sizes=(2, 2), seed=4)
+    step = H.make_step(wl, inp, mode)
+    scores = np.random.default_rng(3).random(step.scores.shape).astype(np.float32)
+    _set_scores(step, scores)
+    step.gather()
+    torch.cuda.synchronize()
+    _check_gather(wl, st, inp, step, scores.astype(np.float64), "NHD")
+    wl0 = wl.replace(top_k=0)
+    step0 = H.make_step(wl0, inp, mode)
+    _set_scores(step0, scores)
+    step0.gather()
+    torch.cuda.synchronize()
+    _check_gather(wl0, st, inp, step0, scores.astype(np.float64), "NHD")
+
+
+def test_many_candidates_radix_select():
+    """Thousands of candidates with heavy ties exercise every radix digit."""
+    wl = synth.tiny_workload(batch=2, chunk_size=16, top_k=700, window=100,
+                             page_size=16)
+    st, inp, mode = H.build_case(wl, ctx_lens=(60000, 9000), tree_sizes=(2, 2),
+                                 seed=8)
+    step = H.make_step(wl, inp, mode)
+    rng = np.random.default_rng(2)
+    s = rng.random(step.scores.shape).astype(np.float32)
+    s[:, ::7] = 0.25                      # a large tie block
+    s[0, 100:110] = np.float32(1e-30)     # tiny positives
+    _set_scores(step, s)
+    step.gather()
+    torch.cuda.synchronize()
+    _check_gather(wl, st, inp, step, s.astype(np.float64), "NHD")
+
+
+@pytest.mark.parametrize("name", ["llama8b-32k", "llama8b-64k"])
+def test_full_size_from_verify_scores(name):
+    wl = synth.WORKLOADS[name]
+    st, inp, mode = H.build_case(wl, layers=1)
+    step = H.make_step(wl, inp, mode)
+    step.verify_layer(0)
+    step.gather()
+    torch.cuda.synchronize()
+    gs = step.scores.double().cpu().numpy()
+    _check_gather(wl, st, inp, step, gs, "NHD")
+    _, rs, _ = H.oracle_layer(wl, st, inp, 0, "NHD", step.max_chunks)
+    for b in range(wl.batch):
+        L = st.ctx_lens[b]
+        got = ref.select_chunks(gs[b], L, wl.chunk_size, wl.top_k, wl.window)
+        want = ref.select_chunks(rs[b], L, wl.chunk_size, wl.top_k, wl.window)
+        if got != want:
+            n = ref.candidate_count(L, wl.chunk_size, wl.window)
+            srt = np.sort(rs[b, :n])[::-1]
+            sk, sk1 = srt[wl.top_k - 1], srt[wl.top_k]
+            assert abs(sk - sk1) <= 1e-3 * sk, "selection differs beyond a near-tie"
+        assert set(st.planted_chunks[b]) <= set(got), "a planted chunk was missed"
