@@ -263,6 +263,10 @@ def run_ours(args, wl, rank, world, local_rank):
     n_ev = args.steps * wl.layers
     evs = [(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    for e_a, e_b in evs:      # torch creates the CUDA event on first record
+        e_a.record()
+        e_b.record()
+    torch.cuda.synchronize()
     prof_args = []
     for i in range(n_ev):
         l = i % wl.layers

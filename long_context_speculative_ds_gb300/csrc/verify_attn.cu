@@ -17,31 +17,15 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "dev_common.cuh"
 #include "internal.h"
+#include "verify_common.cuh"
 
 namespace ds {
 
-struct VerifyKArgs {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  const int32_t* page_table;
-  const int32_t* parents;
-  PlanArgs plan;
-  int32_t num_q_heads, num_pages;
-  int64_t page_stride, tok_stride, head_stride;   // elements
-  float scale_log2;
-  float* o_part;
-  float* lse_part;
-  float* clse;
-  float* row_lse;
-  void* out;
-  int32_t out_f32;
-  float* scores;
-  int32_t accumulate;
-};
+
 
 // ---------------------------------------------------------------------------
 // split pass, CUDA-core version: one thread per query row (<= 256 rows).
@@ -310,10 +294,13 @@ __global__ void __launch_bounds__(256) chunk_finalize(VerifyKArgs a) {
 
 // ---------------------------------------------------------------------------
 
+cudaError_t launch_split_tc(const VerifyKArgs& k, const ds_verify_args& a,
+                            const VerifyLayout& L, cudaStream_t stream);
+
 template <int D>
-static cudaError_t launch_d(const VerifyKArgs& k, const VerifyLayout& L,
-                            int batch, cudaStream_t stream, cudaEvent_t ev0,
-                            cudaEvent_t ev1) {
+static cudaError_t launch_d(const VerifyKArgs& k, const ds_verify_args& a,
+                            const VerifyLayout& L, int batch, cudaStream_t stream,
+                            cudaEvent_t ev0, cudaEvent_t ev1) {
   const size_t smem = 2ull * kTileKeys * D * sizeof(__nv_bfloat16);
   static bool attr_set = false;
   if (!attr_set) {
@@ -323,9 +310,18 @@ static cudaError_t launch_d(const VerifyKArgs& k, const VerifyLayout& L,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  static const bool simt = [] {
+    const char* v = getenv("DS_SPLIT_IMPL");
+    return v && v[0] == 's';
+  }();
   if (ev0) cudaEventRecord(ev0, stream);
-  verify_split_simt<D><<<L.max_items, 256, smem, stream>>>(k);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (simt) {
+    verify_split_simt<D><<<L.max_items, 256, smem, stream>>>(k);
+    e = cudaGetLastError();
+  } else {
+    e = launch_split_tc(k, a, L, stream);
+  }
   if (e != cudaSuccess) return e;
   if (ev1) cudaEventRecord(ev1, stream);
   dim3 gc(batch * k.plan.num_kv_heads * L.rg_max, kRowsPerGroup / 8);
@@ -382,8 +378,8 @@ cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
   k.accumulate = a.accumulate_scores;
   cudaEvent_t ev0 = static_cast<cudaEvent_t>(a.prof_event_start);
   cudaEvent_t ev1 = static_cast<cudaEvent_t>(a.prof_event_stop);
-  if (a.head_dim == 128) return launch_d<128>(k, L, a.batch, stream, ev0, ev1);
-  return launch_d<64>(k, L, a.batch, stream, ev0, ev1);
+  if (a.head_dim == 128) return launch_d<128>(k, a, L, a.batch, stream, ev0, ev1);
+  return launch_d<64>(k, a, L, a.batch, stream, ev0, ev1);
 }
 
 }  // namespace ds

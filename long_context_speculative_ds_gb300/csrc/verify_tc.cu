@@ -1,0 +1,707 @@
+// Split pass of the tree-verify attention on the 5th-generation tensor cores
+// (tcgen05) of sm_103a.
+//
+// One CTA per work item (sequence, kv head, row group of up to 256 query
+// rows, contiguous range of 128-key tiles), 12 warps:
+//   warp 0      loader: Q once, then K and V tiles into shared-memory rings.
+//               Tiles wholly inside the committed context arrive by TMA, one
+//               box per (page, 64-column half); the one or two tiles that
+//               hold tree slots or the end of the sequence are copied with
+//               plain loads so that slots past the sequence end read as zero.
+//   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory, then
+//               O += P V with P read straight from tensor memory.
+//   warp 2      tensor-memory allocator.
+//   warps 4-7   softmax group 0, warps 8-11 softmax group 1: one query row
+//               per thread (its tensor-memory lane).
+// Two independent streams keep the tensor pipe busy while a softmax group
+// works: with more than 128 rows, group g owns rows 128g..128g+127 of every
+// tile ("row mode"); with at most 128 rows both groups use the same rows and
+// take alternate tiles, and their partial results are merged at the end
+// ("key mode").  Tensor memory (512 columns): S of group g at 128g, O of
+// group g at 256 + 128g; P (bf16) overwrites the first 64 columns of S.
+//
+// Softmax works in log2 units with lazy rescaling: the running maximum only
+// moves (and O is rescaled) when a row's new maximum exceeds it by more than
+// 8, so P stays below 2^8.  Per tile each row also writes, for every context
+// chunk in the tile, log2 of its attention mass relative to the row's current
+// maximum (plus that maximum), which the finalize kernel turns into chunk
+// salience; tree keys count toward the softmax denominator only.
+//
+// Every wait is bounded; on a timeout the CTA raises DS_DEV_TIMEOUT, drains
+// what it issued, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "dev_common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+#include "verify_common.cuh"
+
+namespace ds {
+namespace tc {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kHalfBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
+constexpr int kTmemCols = 512;
+
+enum Bar {
+  kQFull = 0,
+  kKFull = 1,      // 3 slots
+  kKEmpty = 4,     // 3 slots
+  kVFull = 7,      // 2 slots
+  kVEmpty = 9,     // 2 slots
+  kSFull = 11,     // 2 groups
+  kPFull = 13,     // 2 groups
+  kOFinal = 15,
+  kNumBars = 16
+};
+
+struct Ctrl {
+  uint64_t bar[kNumBars];
+  uint32_t tmem_base;
+  int abort;
+  Plan plan;
+  int32_t parents[DS_MAX_TREE_NODES];
+  uint64_t anc[DS_MAX_TREE_NODES];
+  float m1[128];
+  float l1[128];
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int TB = 128 * D * 2;   // bytes of one 128-row tile
+  static constexpr int NH = D / 64;        // 128-byte column halves
+  static constexpr size_t smem = 6 * TB + sizeof(Ctrl) + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    verify_split_tc(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const VerifyKArgs a,
+                    const int hnd) {
+  using namespace ptx;
+  constexpr int TB = Cfg<D>::TB;
+  constexpr int NH = Cfg<D>::NH;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t sQ = sbase;             // Q tiles 0, 1
+  const uint32_t sK = sbase + 2 * TB;    // K slots 0, 1 (slot 2 = Q tile 1 in key mode)
+  const uint32_t sV = sbase + 4 * TB;    // V slots 0, 1
+  float* merge_buf = reinterpret_cast<float*>(smem + 4 * TB);   // [D][128], key mode
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + 6 * TB);
+  volatile int* abort_flag = &ctrl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return smem_addr(&ctrl->bar[i]); };
+
+  // ---------------------------------------------------------------- set-up
+  if (warp == 0) {
+    Plan p = plan_find(a.plan, -1, blockIdx.x);
+    if (lane == 0) ctrl->plan = p;
+  } else if (warp == 1 && lane == 0) {
+    mbar_init(bar(kQFull), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kPFull + s), 128);
+    }
+    mbar_init(bar(kOFinal), 1);
+    ctrl->abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  } else if (warp == 2) {
+    tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+  const Plan p = ctrl->plan;
+  const bool active = (int)blockIdx.x < p.total_items && p.b >= 0;
+
+  // work item
+  const SeqPlan& sq = p.seq;
+  const int G = a.plan.group;
+  int h = 0, rgi = 0, t0 = 0, t1 = 0, rows_here = 0;
+  if (active) {
+    const int local = blockIdx.x - sq.item_base;
+    const int per_h = sq.rg * sq.splits;
+    h = local / per_h;
+    rgi = (local % per_h) / sq.splits;
+    const int split = local % sq.splits;
+    t0 = split * p.tps;
+    t1 = min(t0 + p.tps, sq.tiles);
+    rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
+  }
+  const int nt = t1 - t0;
+  const bool row_mode = rows_here > 128;
+  const int L = sq.L, T = sq.T;
+  const bool need_anc = active && t1 * kTileKeys > L;
+
+  if (need_anc && warp == 3) {
+    // ancestor masks of all nodes of this tree, by pointer doubling
+    for (int j = lane; j < T; j += 32) ctrl->parents[j] = __ldg(a.parents + sq.node0 + j);
+    __syncwarp();
+    uint64_t m[2] = {0, 0};
+    int up[2] = {-1, -1};
+    for (int k = 0; k < 2; ++k) {
+      const int j = lane + 32 * k;
+      if (j < T) {
+        int pj = ctrl->parents[j];
+        bool ok = (j == 0) ? (pj == -1) : (pj >= 0 && pj < j);
+        if (!ok) {
+          flag(a.plan.status, DS_DEV_BAD_TREE);
+          pj = -1;
+        }
+        m[k] = (1ull << j) | (pj >= 0 ? (1ull << pj) : 0ull);
+        up[k] = pj;
+        ctrl->anc[j] = m[k];
+        ctrl->parents[j] = pj;   // sanitised jump pointer
+      }
+    }
+    __syncwarp();
+    for (int round = 0; round < 6; ++round) {
+      uint64_t add[2] = {0, 0};
+      int nup[2] = {-1, -1};
+      for (int k = 0; k < 2; ++k) {
+        const int j = lane + 32 * k;
+        if (j < T && up[k] >= 0) {
+          add[k] = ctrl->anc[up[k]];
+          nup[k] = ctrl->parents[up[k]];
+        }
+      }
+      __syncwarp();
+      for (int k = 0; k < 2; ++k) {
+        const int j = lane + 32 * k;
+        if (j < T) {
+          m[k] |= add[k];
+          up[k] = nup[k];
+          ctrl->anc[j] = m[k];
+          ctrl->parents[j] = nup[k];
+        }
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  const int kslots = row_mode ? 2 : 3;
+  const int klead = row_mode ? 1 : 2;
+  auto kslot_addr = [&](int s) -> uint32_t { return s < 2 ? sK + s * TB : sQ + TB; };
+  auto vslot_addr = [&](int s) -> uint32_t { return sV + s * TB; };
+
+  if (warp < 4) {
+    if (!(active && nt > 0)) {
+    } else if (warp == 0) {
+      // ------------------------------------------------------------ loader
+      const int P = a.plan.page_size;
+      const int npg = kTileKeys / P;
+      const int nops = npg * NH;                  // TMA boxes per tile per tensor
+      const int32_t* ptab = a.page_table + (int64_t)p.b * a.plan.max_pages;
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        const int nq = row_mode ? 2 : 1;
+        mbar_arrive_expect_tx(bar(kQFull), nq * TB);
+        for (int qt = 0; qt < nq; ++qt) {
+          const int j0 = (rgi * kRowsPerGroup + qt * 128) / G;
+          for (int hf = 0; hf < NH; ++hf)
+            tma_load_3d(sQ + qt * TB + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, h * G,
+                        sq.node0 + j0);
+        }
+      }
+      // one tile of K (is_v = 0) or V (is_v = 1) into its ring slot
+      auto load_tile = [&](int n, int is_v) -> bool {
+        const int t = t0 + n;
+        const int nslots = is_v ? 2 : kslots;
+        const int slot = n % nslots;
+        const int use = n / nslots;
+        const uint32_t full = bar((is_v ? kVFull : kKFull) + slot);
+        const uint32_t empty = bar((is_v ? kVEmpty : kKEmpty) + slot);
+        const uint32_t dst = is_v ? vslot_addr(slot) : kslot_addr(slot);
+        const int slot0 = t * kTileKeys;
+        const bool full_ctx = slot0 + kTileKeys <= L;
+        int pg = 0;
+        if (full_ctx && lane < nops) {
+          pg = __ldg(ptab + slot0 / P + lane / NH);
+          if (pg < 0 || pg >= a.num_pages) {
+            flag(a.plan.status, DS_DEV_BAD_PAGE);
+            pg = a.num_pages;          // wholly out of bounds: TMA fills zeros
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(empty, (use & 1) ^ 1, abort_flag))) return false;
+        if (full_ctx) {
+          if (lane == 0) mbar_arrive_expect_tx(full, TB);
+          __syncwarp();
+          if (lane < nops) {
+            const int pp = lane / NH, hf = lane % NH;
+            const uint32_t d = dst + hf * kHalfBytes + pp * P * 128;
+            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+            if (hnd)
+              tma_load_4d(d, m, full, hf * 64, 0, h, pg);
+            else
+              tma_load_4d(d, m, full, hf * 64, h, 0, pg);
+          }
+        } else {
+          // tail tile: plain 16-byte loads, zeros past the sequence end,
+          // written in the 128-byte swizzled layout the MMA expects
+          const __nv_bfloat16* src = is_v ? a.v : a.k;
+          constexpr int VPR = D / 8;
+          for (int e = lane; e < kTileKeys * VPR; e += 32) {
+            const int kk = e / VPR, c = e % VPR;
+            const int slot = slot0 + kk;
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (slot < L + T) {
+              int pgi = __ldg(ptab + slot / P);
+              if (pgi >= 0 && pgi < a.num_pages) {
+                const int64_t off = (int64_t)pgi * a.page_stride +
+                                    (int64_t)(slot % P) * a.tok_stride +
+                                    (int64_t)h * a.head_stride + c * 8;
+                x = __ldg(reinterpret_cast<const uint4*>(src + off));
+              } else {
+                flag(a.plan.status, DS_DEV_BAD_PAGE);
+              }
+            }
+            const int hf = c >> 3, c8 = c & 7;
+            const uint32_t d = dst + hf * kHalfBytes + kk * 128 + ((c8 ^ (kk & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(x.x),
+                         "r"(x.y), "r"(x.z), "r"(x.w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full);
+        }
+        return true;
+      };
+      bool ok = true;
+      int nk = 0, nv = 0;   // tiles issued
+      for (int n = 0; ok && n < klead && n < nt; ++n) ok = load_tile(n, 0), nk += ok;
+      for (int n = 0; ok && n < nt; ++n) {
+        ok = load_tile(n, 1);
+        nv += ok;
+        if (ok && n + klead < nt) ok = load_tile(n + klead, 0), nk += ok;
+      }
+      // copies still in flight must land before the CTA can exit
+      if (!ok && lane == 0) {
+        for (int n = max(0, nk - kslots); n < nk; ++n)
+          drain_wait(bar(kKFull + n % kslots), (n / kslots) & 1);
+        for (int n = max(0, nv - 2); n < nv; ++n)
+          drain_wait(bar(kVFull + n % 2), (n / 2) & 1);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+        auto sc = [&](int g) { return tmem + (uint32_t)(g * 128); };
+        auto oc = [&](int g) { return tmem + (uint32_t)(256 + g * 128); };
+        auto qk = [&](int n, int qt, int g) {
+          const uint32_t kb = kslot_addr(n % kslots);
+          const uint32_t qb = sQ + qt * TB;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_ss(sc(g), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                   idesc_qk, kk > 0);
+          }
+        };
+        auto pv = [&](int n, int g, bool acc) {
+          const uint32_t vb = vslot_addr(n % 2);
+#pragma unroll
+          for (int kk = 0; kk < kTileKeys / 16; ++kk)
+            mma_ts(oc(g), sc(g) + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024),
+                   idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        };
+        auto wait_k = [&](int n) {
+          return mbar_wait(bar(kKFull + n % kslots), (n / kslots) & 1, abort_flag);
+        };
+        bool ok = mbar_wait(bar(kQFull), 0, abort_flag) && wait_k(0);
+        if (ok) {
+          tc_fence_after();
+          if (row_mode) {
+            qk(0, 0, 0);
+            mma_commit(bar(kSFull + 0));
+            qk(0, 1, 1);
+            mma_commit(bar(kSFull + 1));
+            mma_commit(bar(kKEmpty + 0));
+            for (int n = 0; ok && n < nt; ++n) {
+              ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag) &&
+                   mbar_wait(bar(kPFull + 0), n & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              pv(n, 0, n > 0);
+              if (n + 1 < nt) {
+                if (!(ok = wait_k(n + 1))) break;
+                tc_fence_after();
+                qk(n + 1, 0, 0);
+                mma_commit(bar(kSFull + 0));
+              }
+              if (!(ok = mbar_wait(bar(kPFull + 1), n & 1, abort_flag))) break;
+              tc_fence_after();
+              pv(n, 1, n > 0);
+              mma_commit(bar(kVEmpty + n % 2));
+              if (n + 1 < nt) {
+                qk(n + 1, 1, 1);
+                mma_commit(bar(kSFull + 1));
+                mma_commit(bar(kKEmpty + (n + 1) % kslots));
+              }
+            }
+          } else {
+            qk(0, 0, 0);
+            mma_commit(bar(kSFull + 0));
+            mma_commit(bar(kKEmpty + 0));
+            if (nt > 1) {
+              ok = wait_k(1);
+              if (ok) {
+                tc_fence_after();
+                qk(1, 0, 1);
+                mma_commit(bar(kSFull + 1));
+                mma_commit(bar(kKEmpty + 1));
+              }
+            }
+            for (int n = 0; ok && n < nt; ++n) {
+              const int g = n & 1;
+              ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag) &&
+                   mbar_wait(bar(kPFull + g), (n >> 1) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              pv(n, g, n >= 2);
+              mma_commit(bar(kVEmpty + n % 2));
+              if (n + 2 < nt) {
+                if (!(ok = wait_k(n + 2))) break;
+                tc_fence_after();
+                qk(n + 2, 0, g);
+                mma_commit(bar(kSFull + g));
+                mma_commit(bar(kKEmpty + (n + 2) % kslots));
+              }
+            }
+          }
+        }
+        // all issued MMAs complete -> epilogue (also on the abort path, so
+        // that nothing is in flight when tensor memory is freed)
+        mma_commit(bar(kOFinal));
+      }
+    }
+  } else {
+    if (active && nt > 0) {
+      // ------------------------------------------------------------ softmax
+      const int g = (warp - 4) >> 2;                 // softmax group
+      const int q4 = warp & 3;                       // TMEM lane quarter
+      const int lrow = q4 * 32 + lane;               // row inside the Q tile
+      const int grow_local = row_mode ? g * 128 + lrow : lrow;
+      const bool row_ok = grow_local < rows_here;
+      const int grow = rgi * kRowsPerGroup + grow_local;
+      const int jn = grow / G;
+      const uint64_t anc = (need_anc && row_ok && jn < T) ? ctrl->anc[jn] : 0ull;
+      const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+      const uint32_t tS = tmem + lane_addr + g * 128;
+      const uint32_t tO = tmem + lane_addr + 256 + g * 128;
+      const float c2 = a.scale_log2;
+      const int C = a.plan.chunk_size;
+      const int n_ch = (L + C - 1) / C;
+      const int64_t clse_row =
+          (((int64_t)p.b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi) *
+              a.plan.max_chunks * kRowsPerGroup + grow_local;
+      float m2 = -CUDART_INF_F, l = 0.f;
+      int my_tiles = 0;
+      bool ok = true;
+      const int first_n = row_mode ? 0 : g;
+      const int step_n = row_mode ? 1 : 2;
+      for (int n = first_n; n < nt; n += step_n, ++my_tiles) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + g), my_tiles & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const int slot0 = (t0 + n) * kTileKeys;
+        const bool tail = slot0 + kTileKeys > L;
+        // column c of a tail tile is visible iff c < L - slot0 (context) or
+        // it is tree slot i = c - (L - slot0) with bit i of the row's
+        // ancestor mask set
+        uint32_t vw[4] = {~0u, ~0u, ~0u, ~0u}, ctxw[4] = {~0u, ~0u, ~0u, ~0u};
+        if (tail) {
+          const int off = L - slot0;
+          typedef unsigned __int128 u128;
+          const u128 ctx = off >= 128 ? ~(u128)0 : (off <= 0 ? (u128)0 : (((u128)1 << off) - 1));
+          u128 tr = (u128)anc;
+          if (off >= 0)
+            tr = off >= 128 ? (u128)0 : (tr << off);
+          else
+            tr = (-off >= 64) ? (u128)0 : (tr >> (-off));
+          const u128 vis = ctx | tr;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            vw[w] = (uint32_t)(vis >> (32 * w));
+            ctxw[w] = (uint32_t)(ctx >> (32 * w));
+          }
+        }
+        // pass 1: row maximum over the visible columns
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tS + half * 64, ra);
+          tmem_ld32(tS + half * 64 + 32, rb);
+          tmem_ld_wait(ra);
+          tmem_ld_wait(rb);
+          const uint32_t wa = vw[2 * half], wb = vw[2 * half + 1];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if ((wa >> i) & 1u) mx = fmaxf(mx, __uint_as_float(ra[i]));
+            if ((wb >> i) & 1u) mx = fmaxf(mx, __uint_as_float(rb[i]));
+          }
+        }
+        const float mx2 = mx * c2;
+        // lazy rescale: move the running maximum only when it grows by > 8
+        float alpha = 1.f;
+        bool rescale = false;
+        if (my_tiles == 0) {
+          m2 = mx2;
+        } else {
+          const bool need = mx2 > m2 + 8.f;
+          rescale = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ex2(m2 - mx2);
+            m2 = mx2;
+          }
+        }
+        const float mb = (m2 == -CUDART_INF_F) ? 0.f : m2;
+        // pass 2: exponentials, row and chunk sums, P (bf16 pairs) written
+        // over the already-consumed S columns: keys 32q..32q+31 -> columns
+        // 16q..16q+15
+        const int per_mask = (C >> 4) - 1;   // 16-column groups per chunk, minus 1
+        float rowsum = 0.f, cs = 0.f;
+        uint32_t rc[32], rn[32];
+        tmem_ld32(tS, rc);
+        tmem_ld_wait(rc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q < 3) tmem_ld32(tS + 32 * (q + 1), rn);
+          uint32_t pk[16];
+          const uint32_t wv = vw[q], wc = ctxw[q];
+#pragma unroll
+          for (int g16 = 0; g16 < 2; ++g16) {
+            float gsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const int c = g16 * 16 + i;
+              const float x0 = ((wv >> c) & 1u) ? ex2(fmaf(__uint_as_float(rc[c]), c2, -mb)) : 0.f;
+              const float x1 = ((wv >> (c + 1)) & 1u) ? ex2(fmaf(__uint_as_float(rc[c + 1]), c2, -mb)) : 0.f;
+              pk[c >> 1] = pack_bf16x2(x0, x1);
+              rowsum += x0 + x1;
+              gsum += (((wc >> c) & 1u) ? x0 : 0.f) + (((wc >> (c + 1)) & 1u) ? x1 : 0.f);
+            }
+            // chunk sums over context columns, emitted at chunk boundaries
+            cs += gsum;
+            const int k = q * 2 + g16;   // 16-column group index in the tile
+            if (((k + 1) & per_mask) == 0) {
+              const int cidx = (slot0 + k * 16) / C;
+              if (row_ok && cidx < n_ch)
+                a.clse[clse_row + (int64_t)cidx * kRowsPerGroup] =
+                    cs > 0.f ? mb + __log2f(cs) : -CUDART_INF_F;
+              cs = 0.f;
+            }
+          }
+          tmem_st16(tS + 16 * q, pk);
+          if (q < 3) {
+            tmem_ld_wait(rn);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rc[i] = rn[i];
+          }
+        }
+        l = l * alpha + rowsum;
+        if (rescale) {
+          // O holds the sum over earlier tiles (their PVs completed before
+          // this tile's S was committed); scale it to the new maximum
+#pragma unroll 1
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t r[32];
+            tmem_ld32(tO + c4 * 32, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + c4 * 32, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kPFull + g));
+      }
+      // ------------------------------------------------------------ epilogue
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFinal), 0, abort_flag));
+      else __syncwarp();
+      if (ok) tc_fence_after();
+      const int nt1 = row_mode ? 0 : nt / 2;       // tiles of group 1 in key mode
+      if (!row_mode && g == 1) {
+        if (ok && nt1 > 0) {
+#pragma unroll 1
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t r[32];
+            tmem_ld32(tO + c4 * 32, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              merge_buf[(c4 * 32 + i) * 128 + lrow] = __uint_as_float(r[i]);
+          }
+        }
+        ctrl->m1[lrow] = m2;
+        ctrl->l1[lrow] = l;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      } else {
+        float sc0 = 1.f, sc1 = 0.f, lt = l, mt = m2;
+        if (!row_mode) {
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (nt1 > 0) {
+            const float m1 = ctrl->m1[lrow], l1 = ctrl->l1[lrow];
+            mt = fmaxf(m2, m1);
+            const float mb2 = (mt == -CUDART_INF_F) ? 0.f : mt;
+            sc0 = l > 0.f ? ex2(m2 - mb2) : 0.f;
+            sc1 = l1 > 0.f ? ex2(m1 - mb2) : 0.f;
+            lt = l * sc0 + l1 * sc1;
+          }
+        }
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        float* op = a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + grow_local) * D;
+#pragma unroll 1
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t r[32];
+          if (ok) {
+            tmem_ld32(tO + c4 * 32, r);
+            tmem_ld_wait(r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float v[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float o = __uint_as_float(r[i + e]) * sc0;
+                if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
+                v[e] = o * inv;
+              }
+              *reinterpret_cast<float4*>(op + c4 * 32 + i) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+          }
+        }
+        if (row_ok)
+          a.lse_part[(int64_t)blockIdx.x * kRowsPerGroup + grow_local] =
+              lt > 0.f ? mt + __log2f(lt) : -CUDART_INF_F;
+      }
+    }
+  }
+
+  // --------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) flag(a.plan.status, DS_DEV_TIMEOUT);
+  if (warp == 2) {
+    if (active && nt > 0 && lane == 0) drain_wait(bar(kOFinal), 0);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_tc(const VerifyKArgs& k, const ds_verify_args& a, const VerifyLayout& L,
+                      cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const int G = L.group;
+  const cuuint64_t P = a.page_size, H = a.num_kv_heads, NP = a.num_pages;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.n_nodes};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_q_heads * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    if (!encode(&tq, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const bool hnd = a.kv_layout == DS_KV_HND;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  if (!hnd) {   // [pages, P, H, D]: dims (D, H, P, pages)
+    cuuint64_t d[4] = {(cuuint64_t)D, H, P, NP};
+    cuuint64_t s[3] = {(cuuint64_t)D * 2, H * D * 2, P * H * D * 2};
+    cuuint32_t b[4] = {64, 1, (cuuint32_t)P, 1};
+    for (int i = 0; i < 4; ++i) { dims[i] = d[i]; box[i] = b[i]; }
+    for (int i = 0; i < 3; ++i) strides[i] = s[i];
+  } else {      // [pages, H, P, D]: dims (D, P, H, pages)
+    cuuint64_t d[4] = {(cuuint64_t)D, P, H, NP};
+    cuuint64_t s[3] = {(cuuint64_t)D * 2, P * D * 2, H * P * D * 2};
+    cuuint32_t b[4] = {64, (cuuint32_t)P, 1, 1};
+    for (int i = 0; i < 4; ++i) { dims[i] = d[i]; box[i] = b[i]; }
+    for (int i = 0; i < 3; ++i) strides[i] = s[i];
+  }
+  if (!encode(&tk, a.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  if (!encode(&tv, a.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  const size_t smem = tc::Cfg<D>::smem;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tc::verify_split_tc<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  tc::verify_split_tc<D><<<L.max_items, tc::kThreads, smem, stream>>>(tq, tk, tv, k, hnd ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_split_tc(const VerifyKArgs& k, const ds_verify_args& a,
+                            const VerifyLayout& L, cudaStream_t stream) {
+  if (a.head_dim == 128) return launch_tc<128>(k, a, L, stream);
+  return launch_tc<64>(k, a, L, stream);
+}
+
+}  // namespace ds
