@@ -46,6 +46,16 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank float over the process group (timings: the job is as
+    slow as its slowest replica)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _kv_bytes(wl, st):
     return sum((L + T) for L, T in zip(st.ctx_lens, st.tree_sizes)) * \
         wl.num_kv_heads * wl.head_dim * 2 * 2
@@ -73,7 +83,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -226,6 +236,41 @@ def _traffic_for(src_path: str):
 
 # ---------------------------------------------------------------------------
 
+def _end_to_end(step, inp, args, world, dev, barrier):
+    """Per step: copy the step's inputs from pinned host memory, run the
+    step through the library, read the results back; wall-clock timed."""
+    import torch
+    from long_context_speculative_ds_gb300.step import StepInputs
+    pin = lambda t: None if t is None else t.cpu().pin_memory()
+    host = StepInputs(
+        page_table=pin(inp.page_table), ctx_lens=pin(inp.ctx_lens),
+        tree_offsets=pin(inp.tree_offsets), parents=pin(inp.parents),
+        q=[pin(x) for x in inp.q], k_cache=[], v_cache=[], src_k=None,
+        src_v=None, target_logits=pin(inp.target_logits),
+        draft_logits=pin(inp.draft_logits), draft_tokens=pin(inp.draft_tokens),
+        uniforms=pin(inp.uniforms))
+    host_out = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory()
+                for n in ("out_path", "out_n", "out_bonus", "out_chunk_ids",
+                          "out_len")}
+    for _ in range(max(1, min(args.warmup, 2))):
+        step.upload(host)
+        step.run()
+        step.download(host_out)
+    torch.cuda.synchronize()
+    barrier()
+    h2d = d2h = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        h2d = step.upload(host)
+        step.run()
+        d2h = step.download(host_out)
+        torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if world > 1:
+        e2e_ms = max_over_ranks(e2e_ms, dev)
+    return e2e_ms, h2d, d2h
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -305,41 +350,11 @@ def run_ours(args, wl, rank, world, local_rank):
     ms = e0.elapsed_time(e1) / args.steps
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
 
     # end to end: pinned host inputs in, results out, every step
-    host = StepInputs(
-        page_table=inp.page_table.cpu().pin_memory(),
-        ctx_lens=inp.ctx_lens.cpu().pin_memory(),
-        tree_offsets=inp.tree_offsets.cpu().pin_memory(),
-        parents=inp.parents.cpu().pin_memory(),
-        q=[x.cpu().pin_memory() for x in inp.q], k_cache=[], v_cache=[],
-        src_k=None, src_v=None,
-        target_logits=inp.target_logits.cpu().pin_memory(),
-        draft_logits=None if inp.draft_logits is None else inp.draft_logits.cpu().pin_memory(),
-        draft_tokens=inp.draft_tokens.cpu().pin_memory(),
-        uniforms=None if inp.uniforms is None else inp.uniforms.cpu().pin_memory())
-    host_out = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory()
-                for n in ("out_path", "out_n", "out_bonus", "out_chunk_ids",
-                          "out_len")}
-    h2d = d2h = 0
-    for _ in range(max(1, min(args.warmup, 2))):
-        step.upload(host); step.run(); step.download(host_out)
-    torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        h2d = step.upload(host)
-        step.run()
-        d2h = step.download(host_out)
-        torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else \
+        _end_to_end(step, inp, args, world, dev, barrier)
     assert step.device_status() == 0
 
     if rank != 0:
@@ -367,7 +382,8 @@ def run_ours(args, wl, rank, world, local_rank):
                      "split_pass_us": round(split_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "traffic": _traffic_for(src)},
-        "e2e": {"value": round(e2e_ms * 1e3 / (wl.layers * world), 3),
+        "e2e": {"value": None if e2e_ms is None else
+                round(e2e_ms * 1e3 / (wl.layers * world), 3),
                 "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "committed and tree K/V stay resident (model state);"
@@ -393,9 +409,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (profiling runs)")
     args = ap.parse_args()
     from long_context_speculative_ds_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.layers:
+        wl = wl.replace(layers=args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
