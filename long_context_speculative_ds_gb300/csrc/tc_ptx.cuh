@@ -45,8 +45,10 @@ DS_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up (and raises *abort) after ~2^31 cycles, or as soon
-// as another role has raised *abort.
-DS_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// as another role has raised *abort.  The first wait of the grid to give up
+// records `where` (a caller-chosen tag) and its block in diag[0..1].
+DS_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                      uint32_t* diag = nullptr, uint32_t where = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -54,6 +56,7 @@ DS_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (*abort) return false;
     if (clock64() - t0 > (1ll << 31)) {
       *abort = 1;
+      if (diag && atomicCAS(diag, 0u, where | 0x80000000u) == 0u) diag[1] = blockIdx.x;
       return false;
     }
   }

@@ -8,24 +8,30 @@
 //               box per (page, 64-column half); the one or two tiles that
 //               hold tree slots or the end of the sequence are copied with
 //               plain loads so that slots past the sequence end read as zero.
-//   warp 1      MMA issuer (one thread): S = Q K^T into tensor memory, then
-//               O += P V with P read straight from tensor memory.
-//   warp 2      tensor-memory allocator.
-//   warps 4-7   softmax group 0, warps 8-11 softmax group 1: one query row
-//               per thread (its tensor-memory lane).
-// Two independent streams keep the tensor pipe busy while a softmax group
-// works: with more than 128 rows, group g owns rows 128g..128g+127 of every
-// tile ("row mode"); with at most 128 rows both groups use the same rows and
-// take alternate tiles, and their partial results are merged at the end
-// ("key mode").  Tensor memory (512 columns): S of group g at 128g, O of
-// group g at 256 + 128g; P (bf16) overwrites the first 64 columns of S.
+//   warp 1      tensor-memory allocator and MMA issuer (one thread).
+//   warps 2-3   idle after set-up.
+//   warps 4-7   softmax group 0, warps 8-11 softmax group 1 (each a whole
+//               warpgroup): one query row per thread, tensor-memory lane
+//               32 * (warp % 4) + lane.
+//
+// Each softmax group owns a stream of 64-key units: with more than 128 rows
+// group g takes rows 128g..128g+127 of every tile ("row mode"); with at most
+// 128 rows both groups use the same rows and take alternate tiles, and their
+// partial results are merged at the end ("key mode").  Tensor memory, 256
+// columns per group: S[0] and S[1] (64 columns each, double-buffered unit
+// scores) and O (128 columns).  For unit u of a group the MMA thread issues
+// S[u % 2] = Q K_u^T; the group turns S into bf16 P over the first 32 columns
+// of the same buffer; the MMA thread issues O += P V_u reading P from tensor
+// memory and immediately refills that buffer with unit u + 2.  A group thus
+// finds its next scores ready when it finishes a unit.
 //
 // Softmax works in log2 units with lazy rescaling: the running maximum only
-// moves (and O is rescaled) when a row's new maximum exceeds it by more than
-// 8, so P stays below 2^8.  Per tile each row also writes, for every context
-// chunk in the tile, log2 of its attention mass relative to the row's current
-// maximum (plus that maximum), which the finalize kernel turns into chunk
-// salience; tree keys count toward the softmax denominator only.
+// moves (and O is rescaled, after the previous P V has completed) when a
+// row's new maximum exceeds it by more than 8, so P stays below 2^8.  For
+// every context chunk each row also writes log2 of the chunk's attention
+// mass relative to the row's maximum (plus that maximum); the finalize kernel
+// turns these into chunk salience.  Tree keys count toward the softmax
+// denominator only.
 //
 // Every wait is bounded; on a timeout the CTA raises DS_DEV_TIMEOUT, drains
 // what it issued, frees its tensor memory and exits.
@@ -45,6 +51,7 @@ namespace tc {
 
 constexpr int kThreads = 384;
 constexpr uint32_t kHalfBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kUnitRowOff = 64 * 128;    // byte offset of key row 64 in a tile half
 constexpr int kTmemCols = 512;
 
 enum Bar {
@@ -53,10 +60,13 @@ enum Bar {
   kKEmpty = 4,     // 3 slots
   kVFull = 7,      // 2 slots
   kVEmpty = 9,     // 2 slots
-  kSFull = 11,     // 2 groups
-  kPFull = 13,     // 2 groups
-  kOFinal = 15,
-  kNumBars = 16
+  kSFull = 11,     // [group][buffer]
+  kPFull = 15,     // [group][buffer]: one barrier per buffer, so that a
+                   // group can never complete two phases of one barrier
+                   // before the MMA thread has seen the first
+  kORdy = 19,      // [group]: one completion per issued P V
+  kOFinal = 21,
+  kNumBars = 22
 };
 
 struct Ctrl {
@@ -68,6 +78,7 @@ struct Ctrl {
   uint64_t anc[DS_MAX_TREE_NODES];
   float m1[128];
   float l1[128];
+  uint32_t where[4];   // last wait site of loader, MMA, softmax groups 0 and 1
 };
 
 template <int D>
@@ -76,6 +87,182 @@ struct Cfg {
   static constexpr int NH = D / 64;        // 128-byte column halves
   static constexpr size_t smem = 6 * TB + sizeof(Ctrl) + 1024;
 };
+
+// One 64-key unit of one softmax thread (one query row): loads the row's 64
+// scores from tensor memory, applies the tree/tail mask (TAIL only), updates
+// the running maximum lazily, writes the exponentials as bf16 P over the
+// first 32 columns of the buffer, and emits the log2 attention mass of every
+// context chunk that ends in this unit.  `cs` carries the context mass of a
+// chunk that started in the previous unit of the same tile.  Returns the
+// factor by which O must be scaled (alpha) and whether any row of the warp
+// needs it.
+template <bool TAIL>
+DS_DEV void softmax_unit(const uint32_t tS, const uint32_t vw0, const uint32_t vw1,
+                         const uint32_t cw0, const uint32_t cw1, const float c2, const bool first,
+                         float& m2, float& l, float& cs, float& alpha, bool& rescale,
+                         const int tile_slot0, const int kbase, const int C, const int n_ch,
+                         const bool row_ok, float* __restrict__ clse_row) {
+  using namespace ptx;
+  float s[64];
+  {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tS, r0);
+    tmem_ld32(tS + 32, r1);
+    tmem_ld_wait(r0);
+    tmem_ld_wait(r1);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      s[i] = __uint_as_float(r0[i]);
+      s[32 + i] = __uint_as_float(r1[i]);
+    }
+  }
+  if constexpr (TAIL) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (!((vw0 >> c) & 1u)) s[c] = -CUDART_INF_F;
+      if (!((vw1 >> c) & 1u)) s[32 + c] = -CUDART_INF_F;
+    }
+  }
+  // row maximum: four independent chains of 16
+  float mx4[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float m = s[16 * k];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) m = fmaxf(m, s[16 * k + i]);
+    mx4[k] = m;
+  }
+  const float mx2 = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+  alpha = 1.f;
+  rescale = false;
+  if (first) {
+    m2 = mx2;
+  } else {
+    const bool need = mx2 > m2 + 8.f;
+    rescale = __any_sync(0xffffffffu, need);
+    if (need) {
+      alpha = ex2(m2 - mx2);
+      m2 = mx2;
+    }
+  }
+  const float mb = (m2 == -CUDART_INF_F) ? 0.f : m2;
+  // exponentials (masked columns: ex2(-inf) = 0) and per-16-column sums of
+  // the context columns; tree columns of a tail unit go to tsum
+  float cg[4];
+  float tsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const int c = 16 * k + i;
+      const float e0 = ex2(fmaf(s[c], c2, -mb));
+      const float e1 = ex2(fmaf(s[c + 1], c2, -mb));
+      s[c] = e0;
+      s[c + 1] = e1;
+      if constexpr (TAIL) {
+        const uint32_t w = c < 32 ? cw0 : cw1;
+        const bool k0 = (w >> (c & 31)) & 1u;
+        const bool k1 = (w >> ((c + 1) & 31)) & 1u;
+        a0 += k0 ? e0 : 0.f;
+        a1 += k1 ? e1 : 0.f;
+        tsum += (k0 ? 0.f : e0) + (k1 ? 0.f : e1);
+      } else {
+        a0 += e0;
+        a1 += e1;
+      }
+    }
+    cg[k] = a0 + a1;
+  }
+  l = l * alpha + (tsum + ((cg[0] + cg[1]) + (cg[2] + cg[3])));
+  // chunk log2-mass at chunk boundaries (C/16 sixteen-column groups a chunk)
+  {
+    const int per_mask = (C >> 4) - 1;
+    cs *= alpha;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      cs += cg[k];
+      const int kg = kbase + k;          // 16-column group index in the tile
+      if (((kg + 1) & per_mask) == 0) {
+        const int cidx = (tile_slot0 + kg * 16) / C;
+        if (row_ok && cidx < n_ch)
+          clse_row[(int64_t)cidx * kRowsPerGroup] = cs > 0.f ? mb + __log2f(cs) : -CUDART_INF_F;
+        cs = 0.f;
+      }
+    }
+  }
+  // P as bf16 pairs over the first 32 columns (keys 2i, 2i+1 -> column i)
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+  tmem_st32(tS, pk);
+}
+
+// Output of one softmax thread after its last tile: O / l (merged with the
+// other group's partial result in key mode) and the row's log2-sum-exp.
+template <int D>
+__device__ __noinline__ void write_row_output(const bool row_mode, const int g, const bool ok,
+                                              const int nt1, const uint32_t tO, const int lrow,
+                                              const bool row_ok, const float m2, const float l,
+                                              float* __restrict__ merge_buf, float* m1buf,
+                                              float* l1buf, float* __restrict__ op,
+                                              float* __restrict__ lse_out) {
+  using namespace ptx;
+  if (!row_mode && g == 1) {
+    if (ok && nt1 > 0) {
+#pragma unroll 1
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(tO + c4 * 32, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) merge_buf[(c4 * 32 + i) * 128 + lrow] = __uint_as_float(r[i]);
+      }
+    }
+    m1buf[lrow] = m2;
+    l1buf[lrow] = l;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    return;
+  }
+  float sc0 = 1.f, sc1 = 0.f, lt = l, mt = m2;
+  if (!row_mode) {
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (nt1 > 0) {
+      const float m1 = m1buf[lrow], l1 = l1buf[lrow];
+      mt = fmaxf(m2, m1);
+      const float mb2 = (mt == -CUDART_INF_F) ? 0.f : mt;
+      sc0 = l > 0.f ? ex2(m2 - mb2) : 0.f;
+      sc1 = l1 > 0.f ? ex2(m1 - mb2) : 0.f;
+      lt = l * sc0 + l1 * sc1;
+    }
+  }
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll 1
+  for (int c4 = 0; c4 < D / 32; ++c4) {
+    uint32_t r[32];
+    if (ok) {
+      tmem_ld32(tO + c4 * 32, r);
+      tmem_ld_wait(r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float o = __uint_as_float(r[i + e]) * sc0;
+          if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
+          v[e] = o * inv;
+        }
+        *reinterpret_cast<float4*>(op + c4 * 32 + i) = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+  }
+  if (row_ok) *lse_out = lt > 0.f ? mt + __log2f(lt) : -CUDART_INF_F;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* merge_buf = reinterpret_cast<float*>(smem + 4 * TB);   // [D][128], key mode
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + 6 * TB);
   volatile int* abort_flag = &ctrl->abort;
+  uint32_t* diag = a.plan.status + 1;   // where a bounded wait gave up
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -114,14 +302,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kORdy + s), 1);
+    }
+    for (int s = 0; s < 4; ++s) {
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kPFull + s), 128);
     }
     mbar_init(bar(kOFinal), 1);
     ctrl->abort = 0;
+    for (int i = 0; i < 4; ++i) ctrl->where[i] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
-  } else if (warp == 2) {
+  }
+  if (warp == 1) {
     tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -135,11 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // work item
   const SeqPlan& sq = p.seq;
   const int G = a.plan.group;
-  int h = 0, rgi = 0, t0 = 0, t1 = 0, rows_here = 0;
+  int kvh = 0, rgi = 0, t0 = 0, t1 = 0, rows_here = 0;
   if (active) {
     const int local = blockIdx.x - sq.item_base;
     const int per_h = sq.rg * sq.splits;
-    h = local / per_h;
+    kvh = local / per_h;
     rgi = (local % per_h) / sq.splits;
     const int split = local % sq.splits;
     t0 = split * p.tps;
@@ -151,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = sq.L, T = sq.T;
   const bool need_anc = active && t1 * kTileKeys > L;
 
-  if (need_anc && warp == 3) {
+  if (need_anc && warp == 0) {
     // ancestor masks of all nodes of this tree, by pointer doubling
     for (int j = lane; j < T; j += 32) ctrl->parents[j] = __ldg(a.parents + sq.node0 + j);
     __syncwarp();
@@ -202,6 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int klead = row_mode ? 1 : 2;
   auto kslot_addr = [&](int s) -> uint32_t { return s < 2 ? sK + s * TB : sQ + TB; };
   auto vslot_addr = [&](int s) -> uint32_t { return sV + s * TB; };
+  // tiles of group g: row mode every tile, key mode every other tile
+  auto ntiles = [&](int g) { return row_mode ? nt : (nt - g + 1) / 2; };
+  auto tile_of = [&](int g, int j) { return row_mode ? j : 2 * j + g; };
 
   if (warp < 4) {
     if (!(active && nt > 0)) {
@@ -220,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int qt = 0; qt < nq; ++qt) {
           const int j0 = (rgi * kRowsPerGroup + qt * 128) / G;
           for (int hf = 0; hf < NH; ++hf)
-            tma_load_3d(sQ + qt * TB + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, h * G,
+            tma_load_3d(sQ + qt * TB + hf * kHalfBytes, &tm_q, bar(kQFull), hf * 64, kvh * G,
                         sq.node0 + j0);
         }
       }
@@ -243,7 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pg = a.num_pages;          // wholly out of bounds: TMA fills zeros
           }
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(empty, (use & 1) ^ 1, abort_flag))) return false;
+        if (lane == 0) ctrl->where[0] = 10000 + (is_v ? kVEmpty : kKEmpty) * 100 + n;
+        if (!__all_sync(0xffffffffu, mbar_wait(empty, (use & 1) ^ 1, abort_flag, diag,
+                                                10000 + (is_v ? kVEmpty : kKEmpty) * 100 + n)))
+          return false;
         if (full_ctx) {
           if (lane == 0) mbar_arrive_expect_tx(full, TB);
           __syncwarp();
@@ -252,9 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t d = dst + hf * kHalfBytes + pp * P * 128;
             const CUtensorMap* m = is_v ? &tm_v : &tm_k;
             if (hnd)
-              tma_load_4d(d, m, full, hf * 64, 0, h, pg);
+              tma_load_4d(d, m, full, hf * 64, 0, kvh, pg);
             else
-              tma_load_4d(d, m, full, hf * 64, h, 0, pg);
+              tma_load_4d(d, m, full, hf * 64, kvh, 0, pg);
           }
         } else {
           // tail tile: plain 16-byte loads, zeros past the sequence end,
@@ -270,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (pgi >= 0 && pgi < a.num_pages) {
                 const int64_t off = (int64_t)pgi * a.page_stride +
                                     (int64_t)(slot % P) * a.tok_stride +
-                                    (int64_t)h * a.head_stride + c * 8;
+                                    (int64_t)kvh * a.head_stride + c * 8;
                 x = __ldg(reinterpret_cast<const uint4*>(src + off));
               } else {
                 flag(a.plan.status, DS_DEV_BAD_PAGE);
@@ -296,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nv += ok;
         if (ok && n + klead < nt) ok = load_tile(n + klead, 0), nk += ok;
       }
+      if (lane == 0) ctrl->where[0] = ok ? 19999 : 19998;
       // copies still in flight must land before the CTA can exit
       if (!ok && lane == 0) {
         for (int n = max(0, nk - kslots); n < nk; ++n)
@@ -306,94 +506,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA
       if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-        auto sc = [&](int g) { return tmem + (uint32_t)(g * 128); };
-        auto oc = [&](int g) { return tmem + (uint32_t)(256 + g * 128); };
-        auto qk = [&](int n, int qt, int g) {
-          const uint32_t kb = kslot_addr(n % kslots);
-          const uint32_t qb = sQ + qt * TB;
+        // S[g][hb] at column 256 g + 64 hb, O[g] at 256 g + 128
+        auto qk = [&](int g, int t, int hb) {
+          const uint32_t kb = kslot_addr(t % kslots) + hb * kUnitRowOff;
+          const uint32_t qb = sQ + (row_mode ? g : 0) * TB;
+          const uint32_t d = tmem + (uint32_t)(256 * g + 64 * hb);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_ss(sc(g), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                   idesc_qk, kk > 0);
+            mma_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk,
+                   kk > 0);
           }
         };
-        auto pv = [&](int n, int g, bool acc) {
-          const uint32_t vb = vslot_addr(n % 2);
+        auto pv = [&](int g, int t, int hb, bool acc) {
+          const uint32_t vb = vslot_addr(t % 2) + hb * kUnitRowOff;
+          const uint32_t d = tmem + (uint32_t)(256 * g + 128);
+          const uint32_t pa = tmem + (uint32_t)(256 * g + 64 * hb);
 #pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk)
-            mma_ts(oc(g), sc(g) + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024),
-                   idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(d, pa + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                   (acc || kk > 0) ? 1u : 0u);
         };
-        auto wait_k = [&](int n) {
-          return mbar_wait(bar(kKFull + n % kslots), (n / kslots) & 1, abort_flag);
+        auto wait_k = [&](int t) {
+          ctrl->where[1] = 20000 + kKFull * 100 + t;
+          return mbar_wait(bar(kKFull + t % kslots), (t / kslots) & 1, abort_flag, diag,
+                           20000 + kKFull * 100 + t);
         };
-        bool ok = mbar_wait(bar(kQFull), 0, abort_flag) && wait_k(0);
-        if (ok) {
-          tc_fence_after();
-          if (row_mode) {
-            qk(0, 0, 0);
-            mma_commit(bar(kSFull + 0));
-            qk(0, 1, 1);
-            mma_commit(bar(kSFull + 1));
-            mma_commit(bar(kKEmpty + 0));
-            for (int n = 0; ok && n < nt; ++n) {
-              ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag) &&
-                   mbar_wait(bar(kPFull + 0), n & 1, abort_flag);
-              if (!ok) break;
+        const int ng = row_mode ? 2 : 1;   // groups that use each tile
+        ctrl->where[1] = 20000 + kQFull * 100;
+        bool ok = mbar_wait(bar(kQFull), 0, abort_flag, diag, 20000 + kQFull * 100);
+        // prologue: both units of each group's first tile
+        for (int g = 0; ok && g < 2; ++g) {
+          if (ntiles(g) == 0) continue;
+          const int t = tile_of(g, 0);
+          if (row_mode ? g == 0 : true) {
+            if (!(ok = wait_k(t))) break;
+            tc_fence_after();
+          }
+          qk(g, t, 0);
+          mma_commit(bar(kSFull + 2 * g + 0));
+          qk(g, t, 1);
+          mma_commit(bar(kSFull + 2 * g + 1));
+          if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + t % kslots));
+        }
+        for (int n = 0; ok && n < nt; ++n) {
+          ctrl->where[1] = 20000 + kVFull * 100 + n;
+          if (!(ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag, diag,
+                               20000 + kVFull * 100 + n)))
+            break;
+          for (int gi = 0; ok && gi < ng; ++gi) {
+            const int g = row_mode ? gi : (n & 1);
+            const int j = row_mode ? n : (n - g) / 2;
+            const bool more = j + 1 < ntiles(g);
+            const int tn = more ? tile_of(g, j + 1) : 0;
+            for (int hb = 0; hb < 2; ++hb) {
+              const int u = 2 * j + hb;
+              ctrl->where[1] = 20000 + (kPFull + 2 * g + hb) * 100 + u;
+              if (!(ok = mbar_wait(bar(kPFull + 2 * g + hb), j & 1, abort_flag, diag,
+                                   20000 + (kPFull + 2 * g + hb) * 100 + u)))
+                break;
               tc_fence_after();
-              pv(n, 0, n > 0);
-              if (n + 1 < nt) {
-                if (!(ok = wait_k(n + 1))) break;
-                tc_fence_after();
-                qk(n + 1, 0, 0);
-                mma_commit(bar(kSFull + 0));
-              }
-              if (!(ok = mbar_wait(bar(kPFull + 1), n & 1, abort_flag))) break;
-              tc_fence_after();
-              pv(n, 1, n > 0);
-              mma_commit(bar(kVEmpty + n % 2));
-              if (n + 1 < nt) {
-                qk(n + 1, 1, 1);
-                mma_commit(bar(kSFull + 1));
-                mma_commit(bar(kKEmpty + (n + 1) % kslots));
-              }
-            }
-          } else {
-            qk(0, 0, 0);
-            mma_commit(bar(kSFull + 0));
-            mma_commit(bar(kKEmpty + 0));
-            if (nt > 1) {
-              ok = wait_k(1);
-              if (ok) {
-                tc_fence_after();
-                qk(1, 0, 1);
-                mma_commit(bar(kSFull + 1));
-                mma_commit(bar(kKEmpty + 1));
-              }
-            }
-            for (int n = 0; ok && n < nt; ++n) {
-              const int g = n & 1;
-              ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag) &&
-                   mbar_wait(bar(kPFull + g), (n >> 1) & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-              pv(n, g, n >= 2);
-              mma_commit(bar(kVEmpty + n % 2));
-              if (n + 2 < nt) {
-                if (!(ok = wait_k(n + 2))) break;
-                tc_fence_after();
-                qk(n + 2, 0, g);
-                mma_commit(bar(kSFull + g));
-                mma_commit(bar(kKEmpty + (n + 2) % kslots));
+              pv(g, n, hb, u > 0);
+              mma_commit(bar(kORdy + g));
+              if (more) {
+                // refill this buffer with unit u + 2 (same half of the
+                // group's next tile)
+                if (hb == 0 && (row_mode ? g == 0 : true)) {
+                  if (!(ok = wait_k(tn))) break;
+                  tc_fence_after();
+                }
+                qk(g, tn, hb);
+                mma_commit(bar(kSFull + 2 * g + hb));
+                if (hb == 1 && (row_mode ? g == 1 : true))
+                  mma_commit(bar(kKEmpty + tn % kslots));
               }
             }
           }
+          if (ok) mma_commit(bar(kVEmpty + n % 2));
         }
         // all issued MMAs complete -> epilogue (also on the abort path, so
         // that nothing is in flight when tensor memory is freed)
+        if (ok) ctrl->where[1] = 29999;
         mma_commit(bar(kOFinal));
       }
     }
@@ -409,209 +604,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jn = grow / G;
       const uint64_t anc = (need_anc && row_ok && jn < T) ? ctrl->anc[jn] : 0ull;
       const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-      const uint32_t tS = tmem + lane_addr + g * 128;
-      const uint32_t tO = tmem + lane_addr + 256 + g * 128;
+      const uint32_t tG = tmem + lane_addr + 256 * g;
+      const uint32_t tO = tG + 128;
       const float c2 = a.scale_log2;
       const int C = a.plan.chunk_size;
       const int n_ch = (L + C - 1) / C;
-      const int64_t clse_row =
-          (((int64_t)p.b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi) *
-              a.plan.max_chunks * kRowsPerGroup + grow_local;
-      float m2 = -CUDART_INF_F, l = 0.f;
-      int my_tiles = 0;
+      float* clse_row = a.clse +
+                        (((int64_t)p.b * a.plan.num_kv_heads + kvh) * a.plan.rg_max + rgi) *
+                            a.plan.max_chunks * kRowsPerGroup +
+                        grow_local;
+      float m2 = -CUDART_INF_F, l = 0.f, cs = 0.f;
       bool ok = true;
-      const int first_n = row_mode ? 0 : g;
-      const int step_n = row_mode ? 1 : 2;
-      for (int n = first_n; n < nt; n += step_n, ++my_tiles) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + g), my_tiles & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const int slot0 = (t0 + n) * kTileKeys;
-        const bool tail = slot0 + kTileKeys > L;
-        // column c of a tail tile is visible iff c < L - slot0 (context) or
-        // it is tree slot i = c - (L - slot0) with bit i of the row's
-        // ancestor mask set
-        uint32_t vw[4] = {~0u, ~0u, ~0u, ~0u}, ctxw[4] = {~0u, ~0u, ~0u, ~0u};
-        if (tail) {
-          const int off = L - slot0;
-          typedef unsigned __int128 u128;
-          const u128 ctx = off >= 128 ? ~(u128)0 : (off <= 0 ? (u128)0 : (((u128)1 << off) - 1));
-          u128 tr = (u128)anc;
-          if (off >= 0)
-            tr = off >= 128 ? (u128)0 : (tr << off);
-          else
-            tr = (-off >= 64) ? (u128)0 : (tr >> (-off));
-          const u128 vis = ctx | tr;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            vw[w] = (uint32_t)(vis >> (32 * w));
-            ctxw[w] = (uint32_t)(ctx >> (32 * w));
+      const int my_nt = ntiles(g);
+      for (int j = 0; ok && j < my_nt; ++j) {
+        const int n = tile_of(g, j);
+        const int tile_slot0 = (t0 + n) * kTileKeys;
+        for (int hb = 0; hb < 2; ++hb) {
+          const int u = 2 * j + hb;
+          if (lrow == 0) ctrl->where[2 + g] = 30000 + (kSFull + 2 * g + hb) * 100 + u;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(kSFull + 2 * g + hb), j & 1, abort_flag, diag,
+                                    30000 + (kSFull + 2 * g + hb) * 100 + u));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tS = tG + 64 * hb;
+          const int unit_slot0 = tile_slot0 + 64 * hb;
+          float alpha;
+          bool rescale;
+          if (unit_slot0 + 64 <= L) {
+            softmax_unit<false>(tS, ~0u, ~0u, ~0u, ~0u, c2, u == 0, m2, l, cs, alpha, rescale,
+                                tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
+          } else {
+            // column c is visible iff c < L - unit_slot0 (context) or it is
+            // tree slot i = c - (L - unit_slot0) with bit i of the row's
+            // ancestor mask set
+            const int off = L - unit_slot0;
+            const uint64_t ctx = off >= 64 ? ~0ull : (off <= 0 ? 0ull : ((1ull << off) - 1));
+            const uint64_t tr = off >= 0 ? (off >= 64 ? 0ull : (anc << off))
+                                         : (-off >= 64 ? 0ull : (anc >> (-off)));
+            const uint64_t vis = ctx | tr;
+            softmax_unit<true>(tS, (uint32_t)vis, (uint32_t)(vis >> 32), (uint32_t)ctx,
+                               (uint32_t)(ctx >> 32), c2, u == 0, m2, l, cs, alpha, rescale,
+                               tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
           }
-        }
-        // pass 1: row maximum over the visible columns
-        float mx = -CUDART_INF_F;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(tS + half * 64, ra);
-          tmem_ld32(tS + half * 64 + 32, rb);
-          tmem_ld_wait(ra);
-          tmem_ld_wait(rb);
-          const uint32_t wa = vw[2 * half], wb = vw[2 * half + 1];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if ((wa >> i) & 1u) mx = fmaxf(mx, __uint_as_float(ra[i]));
-            if ((wb >> i) & 1u) mx = fmaxf(mx, __uint_as_float(rb[i]));
-          }
-        }
-        const float mx2 = mx * c2;
-        // lazy rescale: move the running maximum only when it grows by > 8
-        float alpha = 1.f;
-        bool rescale = false;
-        if (my_tiles == 0) {
-          m2 = mx2;
-        } else {
-          const bool need = mx2 > m2 + 8.f;
-          rescale = __any_sync(0xffffffffu, need);
-          if (need) {
-            alpha = ex2(m2 - mx2);
-            m2 = mx2;
-          }
-        }
-        const float mb = (m2 == -CUDART_INF_F) ? 0.f : m2;
-        // pass 2: exponentials, row and chunk sums, P (bf16 pairs) written
-        // over the already-consumed S columns: keys 32q..32q+31 -> columns
-        // 16q..16q+15
-        const int per_mask = (C >> 4) - 1;   // 16-column groups per chunk, minus 1
-        float rowsum = 0.f, cs = 0.f;
-        uint32_t rc[32], rn[32];
-        tmem_ld32(tS, rc);
-        tmem_ld_wait(rc);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q < 3) tmem_ld32(tS + 32 * (q + 1), rn);
-          uint32_t pk[16];
-          const uint32_t wv = vw[q], wc = ctxw[q];
-#pragma unroll
-          for (int g16 = 0; g16 < 2; ++g16) {
-            float gsum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              const int c = g16 * 16 + i;
-              const float x0 = ((wv >> c) & 1u) ? ex2(fmaf(__uint_as_float(rc[c]), c2, -mb)) : 0.f;
-              const float x1 = ((wv >> (c + 1)) & 1u) ? ex2(fmaf(__uint_as_float(rc[c + 1]), c2, -mb)) : 0.f;
-              pk[c >> 1] = pack_bf16x2(x0, x1);
-              rowsum += x0 + x1;
-              gsum += (((wc >> c) & 1u) ? x0 : 0.f) + (((wc >> (c + 1)) & 1u) ? x1 : 0.f);
-            }
-            // chunk sums over context columns, emitted at chunk boundaries
-            cs += gsum;
-            const int k = q * 2 + g16;   // 16-column group index in the tile
-            if (((k + 1) & per_mask) == 0) {
-              const int cidx = (slot0 + k * 16) / C;
-              if (row_ok && cidx < n_ch)
-                a.clse[clse_row + (int64_t)cidx * kRowsPerGroup] =
-                    cs > 0.f ? mb + __log2f(cs) : -CUDART_INF_F;
-              cs = 0.f;
-            }
-          }
-          tmem_st16(tS + 16 * q, pk);
-          if (q < 3) {
-            tmem_ld_wait(rn);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rc[i] = rn[i];
-          }
-        }
-        l = l * alpha + rowsum;
-        if (rescale) {
-          // O holds the sum over earlier tiles (their PVs completed before
-          // this tile's S was committed); scale it to the new maximum
+          if (rescale) {
+            // O holds the sum over earlier units once the previous P V has
+            // completed; scale it to the new maximum
+            if (lrow == 0) ctrl->where[2 + g] = 30000 + (kORdy + g) * 100 + u;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kORdy + g), (u - 1) & 1, abort_flag, diag,
+                                                   30000 + (kORdy + g) * 100 + u));
+            if (ok) {
+              tc_fence_after();
 #pragma unroll 1
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t r[32];
-            tmem_ld32(tO + c4 * 32, r);
-            tmem_ld_wait(r);
+              for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t r[32];
+                tmem_ld32(tO + c4 * 32, r);
+                tmem_ld_wait(r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + c4 * 32, r);
+                for (int i = 0; i < 32; ++i)
+                  r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(tO + c4 * 32, r);
+              }
+            }
           }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(kPFull + 2 * g + hb));
+          if (!ok) break;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(kPFull + g));
       }
       // ------------------------------------------------------------ epilogue
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFinal), 0, abort_flag));
+      if (lrow == 0) ctrl->where[2 + g] = 30000 + kOFinal * 100;
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(kOFinal), 0, abort_flag, diag, 30000 + kOFinal * 100));
       else __syncwarp();
       if (ok) tc_fence_after();
-      const int nt1 = row_mode ? 0 : nt / 2;       // tiles of group 1 in key mode
-      if (!row_mode && g == 1) {
-        if (ok && nt1 > 0) {
-#pragma unroll 1
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t r[32];
-            tmem_ld32(tO + c4 * 32, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              merge_buf[(c4 * 32 + i) * 128 + lrow] = __uint_as_float(r[i]);
-          }
-        }
-        ctrl->m1[lrow] = m2;
-        ctrl->l1[lrow] = l;
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-      } else {
-        float sc0 = 1.f, sc1 = 0.f, lt = l, mt = m2;
-        if (!row_mode) {
-          asm volatile("bar.sync 1, 256;" ::: "memory");
-          if (nt1 > 0) {
-            const float m1 = ctrl->m1[lrow], l1 = ctrl->l1[lrow];
-            mt = fmaxf(m2, m1);
-            const float mb2 = (mt == -CUDART_INF_F) ? 0.f : mt;
-            sc0 = l > 0.f ? ex2(m2 - mb2) : 0.f;
-            sc1 = l1 > 0.f ? ex2(m1 - mb2) : 0.f;
-            lt = l * sc0 + l1 * sc1;
-          }
-        }
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        float* op = a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + grow_local) * D;
-#pragma unroll 1
-        for (int c4 = 0; c4 < D / 32; ++c4) {
-          uint32_t r[32];
-          if (ok) {
-            tmem_ld32(tO + c4 * 32, r);
-            tmem_ld_wait(r);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              float v[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float o = __uint_as_float(r[i + e]) * sc0;
-                if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
-                v[e] = o * inv;
-              }
-              *reinterpret_cast<float4*>(op + c4 * 32 + i) = make_float4(v[0], v[1], v[2], v[3]);
-            }
-          }
-        }
-        if (row_ok)
-          a.lse_part[(int64_t)blockIdx.x * kRowsPerGroup + grow_local] =
-              lt > 0.f ? mt + __log2f(lt) : -CUDART_INF_F;
-      }
+      const int nt1 = row_mode ? 0 : ntiles(1);    // tiles of group 1 in key mode
+      write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, row_ok, m2, l, merge_buf, ctrl->m1,
+                          ctrl->l1,
+                          a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + grow_local) * D,
+                          a.lse_part + (int64_t)blockIdx.x * kRowsPerGroup + grow_local);
     }
   }
 
   // --------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) flag(a.plan.status, DS_DEV_TIMEOUT);
-  if (warp == 2) {
+  if (*abort_flag && threadIdx.x == 0) {
+    flag(a.plan.status, DS_DEV_TIMEOUT);
+    if (diag[1] == blockIdx.x)
+      for (int i = 0; i < 4; ++i) diag[2 + i] = ctrl->where[i];
+  }
+  if (warp == 1) {
     if (active && nt > 0 && lane == 0) drain_wait(bar(kOFinal), 0);
     __syncwarp();
     tc_fence_after();
