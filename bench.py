@@ -208,8 +208,8 @@ def run_reference(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def _config(wl, st):
-    return {"workload": wl.name, "batch": wl.batch,
+def _config(wl, st, kv_layout="NHD"):
+    return {"workload": wl.name, "batch": wl.batch, "kv_layout": kv_layout,
             "ctx_lens": st.ctx_lens if wl.batch <= 8 else "ragged",
             "tree_nodes": st.tree_sizes, "layers": wl.layers,
             "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
@@ -288,9 +288,9 @@ def run_ours(args, wl, rank, world, local_rank):
     st = synth.make_structure(wl)
     qs, ks, vs = [], [], []
     for l in range(wl.layers):
-        q, k, v = synth.make_layer(st, l, device=dev)
+        q, k, v = synth.make_layer(st, l, device=dev, layout=args.kv_layout)
         qs.append(q); ks.append(k); vs.append(v)
-    sk, sv = synth.make_source_cache(st, device=dev)
+    sk, sv = synth.make_source_cache(st, device=dev, layout=args.kv_layout)
     mode = "reject" if wl.accept == "reject" else "greedy"
     acc = synth.make_accept_inputs(st, mode, device=dev)
     i32 = dict(dtype=torch.int32, device=dev)
@@ -303,7 +303,8 @@ def run_ours(args, wl, rank, world, local_rank):
                      draft_logits=acc.draft_logits,
                      draft_tokens=acc.draft_tokens, uniforms=acc.uniforms)
     step = VerifyStep(inp, chunk_size=wl.chunk_size, top_k=wl.top_k,
-                      window=wl.window, accept_mode=mode)
+                      window=wl.window, accept_mode=mode,
+                      kv_layout=args.kv_layout)
     # per-layer events around the split-pass kernel
     n_ev = args.steps * wl.layers
     evs = [(torch.cuda.Event(enable_timing=True),
@@ -320,7 +321,7 @@ def run_ours(args, wl, rank, world, local_rank):
             inp.ctx_lens, inp.tree_offsets, inp.parents,
             chunk_size=wl.chunk_size, out=step.out[l],
             chunk_scores=step.scores, workspace=step.ws_verify,
-            accumulate=l > 0, prof_events=evs[i]))
+            kv_layout=args.kv_layout, accumulate=l > 0, prof_events=evs[i]))
 
     def barrier():
         if world > 1:
@@ -372,7 +373,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": _config(wl, st),
+        "data": "synthetic", "config": _config(wl, st, args.kv_layout),
         "kv_gbs": round(kv_gbs, 1),
         "hbm_frac": round(kv_gbs / peak, 4),
         "roofline": {"kernel": "verify split pass", "bound": "hbm",
@@ -410,6 +411,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the workload's layer count (profiling runs)")
     args = ap.parse_args()

@@ -14,16 +14,17 @@
 //               warpgroup): one query row per thread, tensor-memory lane
 //               32 * (warp % 4) + lane.
 //
-// Each softmax group owns a stream of 64-key units: with more than 128 rows
-// group g takes rows 128g..128g+127 of every tile ("row mode"); with at most
-// 128 rows both groups use the same rows and take alternate tiles, and their
-// partial results are merged at the end ("key mode").  Tensor memory, 256
-// columns per group: S[0] and S[1] (64 columns each, double-buffered unit
-// scores) and O (128 columns).  For unit u of a group the MMA thread issues
-// S[u % 2] = Q K_u^T; the group turns S into bf16 P over the first 32 columns
-// of the same buffer; the MMA thread issues O += P V_u reading P from tensor
-// memory and immediately refills that buffer with unit u + 2.  A group thus
-// finds its next scores ready when it finishes a unit.
+// Each softmax group owns a stream of 128-key tiles: with more than 128
+// rows group g takes rows 128g..128g+127 of every tile ("row mode"); with at
+// most 128 rows both groups use the same rows and take alternate tiles, and
+// their partial results are merged at the end ("key mode").  Tensor memory,
+// 256 columns per group: S (128 columns) and O (128 columns).  Per tile the
+// MMA thread issues S = Q K^T (one M128 N128 chain); the group turns S into
+// bf16 P in two 64-key halves, P of half h over columns 32h..32h+31, and
+// signals each half separately, so O += P V of the first half runs while the
+// group works on the second; after the second half's P V the MMA thread
+// issues the group's next S.  Two groups keep the tensor pipe busy while
+// either one computes exponentials.
 //
 // Softmax works in log2 units with lazy rescaling: the running maximum only
 // moves (and O is rescaled, after the previous P V has completed) when a
@@ -58,12 +59,13 @@ enum Bar {
   kQFull = 0,
   kKFull = 1,      // 3 slots
   kKEmpty = 4,     // 3 slots
-  kVFull = 7,      // 2 slots
-  kVEmpty = 9,     // 2 slots
-  kSFull = 11,     // [group][buffer]
-  kPFull = 15,     // [group][buffer]: one barrier per buffer, so that a
-                   // group can never complete two phases of one barrier
-                   // before the MMA thread has seen the first
+  kVFull = 7,      // 3 slots
+  kVEmpty = 10,    // 3 slots
+  kSFull = 13,     // [group]: S of the group's next tile is ready
+  kPFull = 15,     // [group][half]: P of one 64-key half is ready; one
+                   // barrier per half, so that a group can never complete
+                   // two phases of one barrier before the MMA thread has
+                   // seen the first
   kORdy = 19,      // [group]: one completion per issued P V
   kOFinal = 21,
   kNumBars = 22
@@ -76,8 +78,6 @@ struct Ctrl {
   Plan plan;
   int32_t parents[DS_MAX_TREE_NODES];
   uint64_t anc[DS_MAX_TREE_NODES];
-  float m1[128];
-  float l1[128];
   uint32_t where[4];   // last wait site of loader, MMA, softmax groups 0 and 1
 };
 
@@ -85,7 +85,8 @@ template <int D>
 struct Cfg {
   static constexpr int TB = 128 * D * 2;   // bytes of one 128-row tile
   static constexpr int NH = D / 64;        // 128-byte column halves
-  static constexpr size_t smem = 6 * TB + sizeof(Ctrl) + 1024;
+  // Q (2 tiles) + K ring (2 slots) + V ring (3 slots) + control block
+  static constexpr size_t smem = 7 * TB + sizeof(Ctrl) + 1024;
 };
 
 // One 64-key unit of one softmax thread (one query row): loads the row's 64
@@ -97,7 +98,8 @@ struct Cfg {
 // factor by which O must be scaled (alpha) and whether any row of the warp
 // needs it.
 template <bool TAIL>
-DS_DEV void softmax_unit(const uint32_t tS, const uint32_t vw0, const uint32_t vw1,
+DS_DEV void softmax_unit(const uint32_t tS, const uint32_t tP, const uint32_t vw0,
+                         const uint32_t vw1,
                          const uint32_t cw0, const uint32_t cw1, const float c2, const bool first,
                          float& m2, float& l, float& cs, float& alpha, bool& rescale,
                          const int tile_slot0, const int kbase, const int C, const int n_ch,
@@ -150,29 +152,45 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t vw0, const uint32_t v
   // the context columns; tree columns of a tail unit go to tsum
   float cg[4];
   float tsum = 0.f;
+  if constexpr (TAIL) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float a0 = 0.f, a1 = 0.f;
+    for (int k = 0; k < 4; ++k) {
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const int c = 16 * k + i;
-      const float e0 = ex2(fmaf(s[c], c2, -mb));
-      const float e1 = ex2(fmaf(s[c + 1], c2, -mb));
-      s[c] = e0;
-      s[c + 1] = e1;
-      if constexpr (TAIL) {
+      for (int i = 0; i < 16; i += 2) {
+        const int c = 16 * k + i;
+        const float e0 = ex2(fmaf(s[c], c2, -mb));
+        const float e1 = ex2(fmaf(s[c + 1], c2, -mb));
+        s[c] = e0;
+        s[c + 1] = e1;
         const uint32_t w = c < 32 ? cw0 : cw1;
         const bool k0 = (w >> (c & 31)) & 1u;
         const bool k1 = (w >> ((c + 1) & 31)) & 1u;
         a0 += k0 ? e0 : 0.f;
         a1 += k1 ? e1 : 0.f;
         tsum += (k0 ? 0.f : e0) + (k1 ? 0.f : e1);
-      } else {
-        a0 += e0;
-        a1 += e1;
       }
+      cg[k] = a0 + a1;
     }
-    cg[k] = a0 + a1;
+  } else {
+    // pairs of columns in f32x2 arithmetic: (s c2 - mb) and the running sums
+    const uint64_t c2x2 = f2pack(c2, c2), nmb2 = f2pack(-mb, -mb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t acc = f2pack(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        const int c = 16 * k + i;
+        float x0, x1;
+        f2unpack(ffma2(f2pack(s[c], s[c + 1]), c2x2, nmb2), x0, x1);
+        s[c] = ex2(x0);
+        s[c + 1] = ex2(x1);
+        acc = fadd2(acc, f2pack(s[c], s[c + 1]));
+      }
+      float lo, hi;
+      f2unpack(acc, lo, hi);
+      cg[k] = lo + hi;
+    }
   }
   l = l * alpha + (tsum + ((cg[0] + cg[1]) + (cg[2] + cg[3])));
   // chunk log2-mass at chunk boundaries (C/16 sixteen-column groups a chunk)
@@ -191,11 +209,11 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t vw0, const uint32_t v
       }
     }
   }
-  // P as bf16 pairs over the first 32 columns (keys 2i, 2i+1 -> column i)
+  // P as bf16 pairs (keys 2i, 2i+1 -> column i of tP)
   uint32_t pk[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-  tmem_st32(tS, pk);
+  tmem_st32(tP, pk);
 }
 
 // Output of one softmax thread after its last tile: O / l (merged with the
@@ -279,9 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t sQ = sbase;             // Q tiles 0, 1
   const uint32_t sK = sbase + 2 * TB;    // K slots 0, 1 (slot 2 = Q tile 1 in key mode)
-  const uint32_t sV = sbase + 4 * TB;    // V slots 0, 1
-  float* merge_buf = reinterpret_cast<float*>(smem + 4 * TB);   // [D][128], key mode
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + 6 * TB);
+  const uint32_t sV = sbase + 4 * TB;    // V slots 0, 1, 2
+  // key-mode merge scratch, used once the V ring is idle: O of group 1
+  // [D][128] f32 and its row maxima and sums
+  float* merge_buf = reinterpret_cast<float*>(smem + 4 * TB);
+  float* m1buf = reinterpret_cast<float*>(smem + 6 * TB);
+  float* l1buf = m1buf + 128;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + 7 * TB);
   volatile int* abort_flag = &ctrl->abort;
   uint32_t* diag = a.plan.status + 1;   // where a bounded wait gave up
 
@@ -299,15 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kKFull + s), 1);
       mbar_init(bar(kKEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kORdy + s), 1);
-    }
-    for (int s = 0; s < 4; ++s) {
       mbar_init(bar(kSFull + s), 1);
-      mbar_init(bar(kPFull + s), 128);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(bar(kPFull + s), 128);
     mbar_init(bar(kOFinal), 1);
     ctrl->abort = 0;
     for (int i = 0; i < 4; ++i) ctrl->where[i] = 0;
@@ -423,63 +445,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one tile of K (is_v = 0) or V (is_v = 1) into its ring slot
       auto load_tile = [&](int n, int is_v) -> bool {
         const int t = t0 + n;
-        const int nslots = is_v ? 2 : kslots;
+        const int nslots = is_v ? 3 : kslots;
         const int slot = n % nslots;
         const int use = n / nslots;
         const uint32_t full = bar((is_v ? kVFull : kKFull) + slot);
         const uint32_t empty = bar((is_v ? kVEmpty : kKEmpty) + slot);
         const uint32_t dst = is_v ? vslot_addr(slot) : kslot_addr(slot);
         const int slot0 = t * kTileKeys;
-        const bool full_ctx = slot0 + kTileKeys <= L;
+        const int valid_end = L + T;           // slots below this hold real keys
+        // Every page of the tile arrives by TMA except a page that holds the
+        // sequence end (partially valid), which is copied with plain loads
+        // so that its slots past the end read as zero.  Pages wholly past the
+        // end get an out-of-range page coordinate: TMA fills them with zeros.
         int pg = 0;
-        if (full_ctx && lane < nops) {
-          pg = __ldg(ptab + slot0 / P + lane / NH);
-          if (pg < 0 || pg >= a.num_pages) {
-            flag(a.plan.status, DS_DEV_BAD_PAGE);
-            pg = a.num_pages;          // wholly out of bounds: TMA fills zeros
+        bool lane_tma = false;
+        if (lane < nops) {
+          const int ps = slot0 + (lane / NH) * P;
+          if (ps + P <= valid_end) {
+            pg = __ldg(ptab + ps / P);
+            if (pg < 0 || pg >= a.num_pages) {
+              flag(a.plan.status, DS_DEV_BAD_PAGE);
+              pg = a.num_pages;
+            }
+            lane_tma = true;
+          } else if (ps >= valid_end) {
+            pg = a.num_pages;
+            lane_tma = true;
           }
         }
+        const uint32_t tma_lanes = __ballot_sync(0xffffffffu, lane_tma);
+        const bool partial = __popc(tma_lanes) != nops;
         if (lane == 0) ctrl->where[0] = 10000 + (is_v ? kVEmpty : kKEmpty) * 100 + n;
         if (!__all_sync(0xffffffffu, mbar_wait(empty, (use & 1) ^ 1, abort_flag, diag,
                                                 10000 + (is_v ? kVEmpty : kKEmpty) * 100 + n)))
           return false;
-        if (full_ctx) {
-          if (lane == 0) mbar_arrive_expect_tx(full, TB);
-          __syncwarp();
-          if (lane < nops) {
-            const int pp = lane / NH, hf = lane % NH;
-            const uint32_t d = dst + hf * kHalfBytes + pp * P * 128;
-            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-            if (hnd)
-              tma_load_4d(d, m, full, hf * 64, 0, kvh, pg);
-            else
-              tma_load_4d(d, m, full, hf * 64, kvh, 0, pg);
-          }
-        } else {
-          // tail tile: plain 16-byte loads, zeros past the sequence end,
-          // written in the 128-byte swizzled layout the MMA expects
+        if (lane == 0) {
+          if (partial)
+            mbar_expect_tx(full, __popc(tma_lanes) * P * 128);
+          else
+            mbar_arrive_expect_tx(full, TB);
+        }
+        __syncwarp();
+        if (lane_tma) {
+          const int pp = lane / NH, hf = lane % NH;
+          const uint32_t d = dst + hf * kHalfBytes + pp * P * 128;
+          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+          if (hnd)
+            tma_load_4d(d, m, full, hf * 64, 0, kvh, pg);
+          else
+            tma_load_4d(d, m, full, hf * 64, kvh, 0, pg);
+        }
+        if (partial) {
+          // the one page with ps < valid_end < ps + P: plain 16-byte loads,
+          // zeros past the end, written in the 128-byte swizzled layout
+          const int pidx = (valid_end - slot0) / P;        // page index in the tile
+          const int ps = slot0 + pidx * P;
+          int pgi = __ldg(ptab + ps / P);
+          const bool pg_ok = pgi >= 0 && pgi < a.num_pages;
+          if (!pg_ok && lane == 0) flag(a.plan.status, DS_DEV_BAD_PAGE);
           const __nv_bfloat16* src = is_v ? a.v : a.k;
-          constexpr int VPR = D / 8;
-          for (int e = lane; e < kTileKeys * VPR; e += 32) {
-            const int kk = e / VPR, c = e % VPR;
-            const int slot = slot0 + kk;
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (slot < L + T) {
-              int pgi = __ldg(ptab + slot / P);
-              if (pgi >= 0 && pgi < a.num_pages) {
-                const int64_t off = (int64_t)pgi * a.page_stride +
-                                    (int64_t)(slot % P) * a.tok_stride +
-                                    (int64_t)kvh * a.head_stride + c * 8;
-                x = __ldg(reinterpret_cast<const uint4*>(src + off));
-              } else {
-                flag(a.plan.status, DS_DEV_BAD_PAGE);
+          constexpr int VPR = D / 8;                         // 16-byte chunks per row
+          const int nelem = P * VPR;
+          for (int base = 0; base < nelem; base += 32 * 8) {
+            uint4 x[8];                                      // 8 loads in flight per lane
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int e = base + lane + 32 * r;
+              x[r] = make_uint4(0, 0, 0, 0);
+              if (e < nelem) {
+                const int row = e / VPR, c = e % VPR;
+                if (pg_ok && ps + row < valid_end) {
+                  const int64_t off = (int64_t)pgi * a.page_stride +
+                                      (int64_t)row * a.tok_stride +
+                                      (int64_t)kvh * a.head_stride + c * 8;
+                  x[r] = __ldg(reinterpret_cast<const uint4*>(src + off));
+                }
               }
             }
-            const int hf = c >> 3, c8 = c & 7;
-            const uint32_t d = dst + hf * kHalfBytes + kk * 128 + ((c8 ^ (kk & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(x.x),
-                         "r"(x.y), "r"(x.z), "r"(x.w)
-                         : "memory");
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int e = base + lane + 32 * r;
+              if (e < nelem) {
+                const int kk = pidx * P + e / VPR, c = e % VPR;
+                const int hf = c >> 3, c8 = c & 7;
+                const uint32_t d = dst + hf * kHalfBytes + kk * 128 + ((c8 ^ (kk & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(x[r].x),
+                             "r"(x[r].y), "r"(x[r].z), "r"(x[r].w)
+                             : "memory");
+              }
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -500,44 +554,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) {
         for (int n = max(0, nk - kslots); n < nk; ++n)
           drain_wait(bar(kKFull + n % kslots), (n / kslots) & 1);
-        for (int n = max(0, nv - 2); n < nv; ++n)
-          drain_wait(bar(kVFull + n % 2), (n / 2) & 1);
+        for (int n = max(0, nv - 3); n < nv; ++n)
+          drain_wait(bar(kVFull + n % 3), (n / 3) & 1);
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA
       if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, false);
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-        // S[g][hb] at column 256 g + 64 hb, O[g] at 256 g + 128
-        auto qk = [&](int g, int t, int hb) {
-          const uint32_t kb = kslot_addr(t % kslots) + hb * kUnitRowOff;
-          const uint32_t qb = sQ + (row_mode ? g : 0) * TB;
-          const uint32_t d = tmem + (uint32_t)(256 * g + 64 * hb);
+        // Descriptor bases computed once; each MMA only adds a compile-time
+        // offset to the 14-bit start-address field (addresses stay below
+        // 256 KB, so the add never carries into the neighbouring fields).
+        const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t qdg = row_mode ? qd0 + (TB >> 4) : qd0;   // Q of group 1
+        const uint64_t kd0 = sdesc_sw128(sK, 16, 1024);
+        const uint64_t kd2 = sdesc_sw128(sQ + TB, 16, 1024);      // K slot 2 (key mode)
+        const uint64_t vd0 = sdesc_sw128(sV, kHalfBytes, 1024);
+        auto kslot_of = [&](int t) { return row_mode ? (t & 1) : (t % 3); };
+        auto kuse_of = [&](int t) { return row_mode ? (t >> 1) : (t / 3); };
+        // S[g] at column 256 g (128 columns), O[g] at 256 g + 128
+        auto qk = [&](int g, int t) {
+          const int ks = kslot_of(t);
+          const uint64_t kb = ks < 2 ? kd0 + (uint64_t)(ks * (TB >> 4)) : kd2;
+          const uint64_t qb = g ? qdg : qd0;
+          const uint32_t d = tmem + (uint32_t)(256 * g);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_ss(d, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk,
-                   kk > 0);
+            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_ss(d, qb + off, kb + off, idesc_qk, kk > 0);
           }
         };
+        // O[g] += P(half hb) V(keys 64 hb .. 64 hb + 63)
         auto pv = [&](int g, int t, int hb, bool acc) {
-          const uint32_t vb = vslot_addr(t % 2) + hb * kUnitRowOff;
+          const uint64_t vb = vd0 + (uint64_t)((t % 3) * (TB >> 4) + hb * (kUnitRowOff >> 4));
           const uint32_t d = tmem + (uint32_t)(256 * g + 128);
-          const uint32_t pa = tmem + (uint32_t)(256 * g + 64 * hb);
+          const uint32_t pa = tmem + (uint32_t)(256 * g + 32 * hb);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(d, pa + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc_pv,
+            mma_ts(d, pa + kk * 8, vb + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                    (acc || kk > 0) ? 1u : 0u);
         };
         auto wait_k = [&](int t) {
           ctrl->where[1] = 20000 + kKFull * 100 + t;
-          return mbar_wait(bar(kKFull + t % kslots), (t / kslots) & 1, abort_flag, diag,
+          return mbar_wait(bar(kKFull + kslot_of(t)), kuse_of(t) & 1, abort_flag, diag,
                            20000 + kKFull * 100 + t);
         };
         const int ng = row_mode ? 2 : 1;   // groups that use each tile
         ctrl->where[1] = 20000 + kQFull * 100;
         bool ok = mbar_wait(bar(kQFull), 0, abort_flag, diag, 20000 + kQFull * 100);
-        // prologue: both units of each group's first tile
+        // prologue: S of each group's first tile
         for (int g = 0; ok && g < 2; ++g) {
           if (ntiles(g) == 0) continue;
           const int t = tile_of(g, 0);
@@ -545,46 +610,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_k(t))) break;
             tc_fence_after();
           }
-          qk(g, t, 0);
-          mma_commit(bar(kSFull + 2 * g + 0));
-          qk(g, t, 1);
-          mma_commit(bar(kSFull + 2 * g + 1));
-          if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + t % kslots));
+          qk(g, t);
+          mma_commit(bar(kSFull + g));
+          if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + kslot_of(t)));
         }
         for (int n = 0; ok && n < nt; ++n) {
           ctrl->where[1] = 20000 + kVFull * 100 + n;
-          if (!(ok = mbar_wait(bar(kVFull + n % 2), (n / 2) & 1, abort_flag, diag,
+          if (!(ok = mbar_wait(bar(kVFull + n % 3), (n / 3) & 1, abort_flag, diag,
                                20000 + kVFull * 100 + n)))
             break;
           for (int gi = 0; ok && gi < ng; ++gi) {
             const int g = row_mode ? gi : (n & 1);
             const int j = row_mode ? n : (n - g) / 2;
-            const bool more = j + 1 < ntiles(g);
-            const int tn = more ? tile_of(g, j + 1) : 0;
             for (int hb = 0; hb < 2; ++hb) {
-              const int u = 2 * j + hb;
-              ctrl->where[1] = 20000 + (kPFull + 2 * g + hb) * 100 + u;
+              ctrl->where[1] = 20000 + (kPFull + 2 * g + hb) * 100 + 2 * j + hb;
               if (!(ok = mbar_wait(bar(kPFull + 2 * g + hb), j & 1, abort_flag, diag,
-                                   20000 + (kPFull + 2 * g + hb) * 100 + u)))
+                                   20000 + (kPFull + 2 * g + hb) * 100 + 2 * j + hb)))
                 break;
               tc_fence_after();
-              pv(g, n, hb, u > 0);
+              pv(g, n, hb, j > 0 || hb > 0);
               mma_commit(bar(kORdy + g));
-              if (more) {
-                // refill this buffer with unit u + 2 (same half of the
-                // group's next tile)
-                if (hb == 0 && (row_mode ? g == 0 : true)) {
-                  if (!(ok = wait_k(tn))) break;
-                  tc_fence_after();
-                }
-                qk(g, tn, hb);
-                mma_commit(bar(kSFull + 2 * g + hb));
-                if (hb == 1 && (row_mode ? g == 1 : true))
-                  mma_commit(bar(kKEmpty + tn % kslots));
+            }
+            if (!ok) break;
+            if (j + 1 < ntiles(g)) {
+              // S is free once this tile's P V has been issued (in-order pipe)
+              const int tn = tile_of(g, j + 1);
+              if (row_mode ? g == 0 : true) {
+                if (!(ok = wait_k(tn))) break;
+                tc_fence_after();
               }
+              qk(g, tn);
+              mma_commit(bar(kSFull + g));
+              if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + kslot_of(tn)));
             }
           }
-          if (ok) mma_commit(bar(kVEmpty + n % 2));
+          if (ok) mma_commit(bar(kVEmpty + n % 3));
         }
         // all issued MMAs complete -> epilogue (also on the abort path, so
         // that nothing is in flight when tensor memory is freed)
@@ -619,21 +679,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < my_nt; ++j) {
         const int n = tile_of(g, j);
         const int tile_slot0 = (t0 + n) * kTileKeys;
+        if (lrow == 0) ctrl->where[2 + g] = 30000 + (kSFull + g) * 100 + j;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + g), j & 1, abort_flag, diag,
+                                               30000 + (kSFull + g) * 100 + j));
+        if (!ok) break;
+        tc_fence_after();
         for (int hb = 0; hb < 2; ++hb) {
           const int u = 2 * j + hb;
-          if (lrow == 0) ctrl->where[2 + g] = 30000 + (kSFull + 2 * g + hb) * 100 + u;
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar(kSFull + 2 * g + hb), j & 1, abort_flag, diag,
-                                    30000 + (kSFull + 2 * g + hb) * 100 + u));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t tS = tG + 64 * hb;
+          const uint32_t tS = tG + 64 * hb;     // scores of keys 64 hb .. 64 hb + 63
+          const uint32_t tP = tG + 32 * hb;     // their P (bf16 pairs)
           const int unit_slot0 = tile_slot0 + 64 * hb;
           float alpha;
           bool rescale;
           if (unit_slot0 + 64 <= L) {
-            softmax_unit<false>(tS, ~0u, ~0u, ~0u, ~0u, c2, u == 0, m2, l, cs, alpha, rescale,
-                                tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
+            softmax_unit<false>(tS, tP, ~0u, ~0u, ~0u, ~0u, c2, u == 0, m2, l, cs, alpha,
+                                rescale, tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
           } else {
             // column c is visible iff c < L - unit_slot0 (context) or it is
             // tree slot i = c - (L - unit_slot0) with bit i of the row's
@@ -643,16 +703,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t tr = off >= 0 ? (off >= 64 ? 0ull : (anc << off))
                                          : (-off >= 64 ? 0ull : (anc >> (-off)));
             const uint64_t vis = ctx | tr;
-            softmax_unit<true>(tS, (uint32_t)vis, (uint32_t)(vis >> 32), (uint32_t)ctx,
+            softmax_unit<true>(tS, tP, (uint32_t)vis, (uint32_t)(vis >> 32), (uint32_t)ctx,
                                (uint32_t)(ctx >> 32), c2, u == 0, m2, l, cs, alpha, rescale,
                                tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
           }
           if (rescale) {
-            // O holds the sum over earlier units once the previous P V has
-            // completed; scale it to the new maximum
-            if (lrow == 0) ctrl->where[2 + g] = 30000 + (kORdy + g) * 100 + u;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kORdy + g), (u - 1) & 1, abort_flag, diag,
-                                                   30000 + (kORdy + g) * 100 + u));
+            // O must hold the sum over all earlier halves: before the first
+            // half that is guaranteed (this S was issued after the previous
+            // P V); before the second half wait for the first half's P V
+            if (hb == 1) {
+              if (lrow == 0) ctrl->where[2 + g] = 30000 + (kORdy + g) * 100 + u;
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(kORdy + g), (u - 1) & 1, abort_flag,
+                                                     diag, 30000 + (kORdy + g) * 100 + u));
+            }
             if (ok) {
               tc_fence_after();
 #pragma unroll 1
@@ -681,8 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else __syncwarp();
       if (ok) tc_fence_after();
       const int nt1 = row_mode ? 0 : ntiles(1);    // tiles of group 1 in key mode
-      write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, row_ok, m2, l, merge_buf, ctrl->m1,
-                          ctrl->l1,
+      write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, row_ok, m2, l, merge_buf, m1buf,
+                          l1buf,
                           a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + grow_local) * D,
                           a.lse_part + (int64_t)blockIdx.x * kRowsPerGroup + grow_local);
     }
