@@ -1,8 +1,9 @@
 // Tree-verify attention over a paged bf16 KV cache with fused chunk salience.
 //
 // Three launches per call:
-//   1. split pass   one CTA per work item (sequence, kv head, row group, split
-//                   of key tiles): online softmax over its key tiles, writing
+//   1. split pass   (tcgen05 kernel in verify_tc.cu) one CTA per work item
+//                   (sequence, kv head, row group, split of key tiles):
+//                   online softmax over its key tiles, writing
 //                   the split's normalised output, its row log2-sum-exp, and
 //                   for every context chunk in its range the chunk's log2
 //                   attention mass per row (log2 sum_{t in chunk} 2^{s_t}).
@@ -17,7 +18,6 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 #include <stdint.h>
-#include <stdlib.h>
 
 #include "dev_common.cuh"
 #include "internal.h"
@@ -25,177 +25,10 @@
 
 namespace ds {
 
-
-
 // ---------------------------------------------------------------------------
-// split pass, CUDA-core version: one thread per query row (<= 256 rows).
-template <int D>
-__global__ void __launch_bounds__(256, 1) verify_split_simt(VerifyKArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(smem);          // [128][D]
-  __nv_bfloat16* sv = sk + kTileKeys * D;                               // [128][D]
-  __shared__ Plan s_plan;
-  __shared__ int32_t s_pages[kTileKeys / 16 * 8];
-
-  if (threadIdx.x < 32) {
-    Plan p = plan_find(a.plan, -1, blockIdx.x);
-    if (threadIdx.x == 0) s_plan = p;
-  }
-  __syncthreads();
-  const Plan p = s_plan;
-  if ((int)blockIdx.x >= p.total_items || p.b < 0) return;
-  const SeqPlan& sq = p.seq;
-  const int G = a.plan.group;
-  const int item = blockIdx.x;
-  const int local = item - sq.item_base;
-  const int per_h = sq.rg * sq.splits;
-  const int h = local / per_h;
-  const int rgi = (local % per_h) / sq.splits;
-  const int split = local % sq.splits;
-  const int t0 = split * p.tps;
-  const int t1 = min(t0 + p.tps, sq.tiles);
-  const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
-  const int r = threadIdx.x;
-  const bool row_ok = r < rows_here;
-  const int grow = rgi * kRowsPerGroup + r;
-  const int j = grow / G;
-  const int qh = h * G + grow % G;
-  const int L = sq.L, T = sq.T;
-  const int n_ch = (L + a.plan.chunk_size - 1) / a.plan.chunk_size;
-  const int C = a.plan.chunk_size;
-  const int b = p.b;
-
-  __nv_bfloat162 q2[D / 2];
-  if (row_ok) {
-    const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(
-        a.q + ((int64_t)(sq.node0 + j) * a.num_q_heads + qh) * D);
-#pragma unroll
-    for (int i = 0; i < D / 2; ++i) q2[i] = src[i];
-  } else {
-#pragma unroll
-    for (int i = 0; i < D / 2; ++i) q2[i] = __floats2bfloat162_rn(0.f, 0.f);
-  }
-  uint64_t anc = 0;
-  if (row_ok && t1 * kTileKeys > L)
-    anc = ancestor_mask(a.parents + sq.node0, j, T, a.plan.status);
-
-  float o[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) o[d] = 0.f;
-  float m = -CUDART_INF_F, l = 0.f, csum = 0.f;
-
-  const int npg_tile = kTileKeys / a.plan.page_size;
-  const int32_t* ptab = a.page_table + (int64_t)b * a.plan.max_pages;
-  for (int t = t0; t < t1; ++t) {
-    const int slot0 = t * kTileKeys;
-    if (threadIdx.x < npg_tile) {
-      int pi = slot0 / a.plan.page_size + threadIdx.x;
-      int pg = -1;
-      if (pi * a.plan.page_size < L + T) {
-        pg = __ldg(ptab + pi);
-        if (pg < 0 || pg >= a.num_pages) {
-          flag(a.plan.status, DS_DEV_BAD_PAGE);
-          pg = -1;
-        }
-      }
-      s_pages[threadIdx.x] = pg;
-    }
-    __syncthreads();
-    // cooperative load of K and V tiles (16-byte vectors), zeros where invalid
-    constexpr int VPR = D / 8;   // vectors per key row
-    for (int e = threadIdx.x; e < kTileKeys * VPR; e += blockDim.x) {
-      int kk = e / VPR, vv = e % VPR;
-      int slot = slot0 + kk;
-      int pg = s_pages[kk / a.plan.page_size];
-      uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
-      if (pg >= 0 && slot < L + T) {
-        int64_t off = (int64_t)pg * a.page_stride +
-                      (int64_t)(slot % a.plan.page_size) * a.tok_stride +
-                      (int64_t)h * a.head_stride + vv * 8;
-        kx = *reinterpret_cast<const uint4*>(a.k + off);
-        vx = *reinterpret_cast<const uint4*>(a.v + off);
-      }
-      reinterpret_cast<uint4*>(sk)[kk * VPR + vv] = kx;
-      reinterpret_cast<uint4*>(sv)[kk * VPR + vv] = vx;
-    }
-    __syncthreads();
-    if (row_ok) {
-      for (int sb = 0; sb < kTileKeys / 16; ++sb) {
-        float s[16];
-        float mloc = -CUDART_INF_F;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const int key = sb * 16 + kk;
-          const int slot = slot0 + key;
-          bool vis = slot < L || (slot < L + T && ((anc >> (slot - L)) & 1ull));
-          const __nv_bfloat162* kr =
-              reinterpret_cast<const __nv_bfloat162*>(sk + key * D);
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < D / 2; ++i) {
-            float2 a2 = __bfloat1622float2(q2[i]);
-            float2 b2 = __bfloat1622float2(kr[i]);
-            acc = fmaf(a2.x, b2.x, acc);
-            acc = fmaf(a2.y, b2.y, acc);
-          }
-          s[kk] = vis ? acc * a.scale_log2 : -CUDART_INF_F;
-          mloc = fmaxf(mloc, s[kk]);
-        }
-        const float mn = fmaxf(m, mloc);
-        if (mn != -CUDART_INF_F) {
-          if (mn > m) {
-            const float alpha = exp2f(m - mn);
-            l *= alpha;
-            csum *= alpha;
-#pragma unroll
-            for (int d = 0; d < D; ++d) o[d] *= alpha;
-            m = mn;
-          }
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const int key = sb * 16 + kk;
-            const float pk = exp2f(s[kk] - m);
-            l += pk;
-            if (slot0 + key < L) csum += pk;
-            const __nv_bfloat162* vr =
-                reinterpret_cast<const __nv_bfloat162*>(sv + key * D);
-#pragma unroll
-            for (int i = 0; i < D / 2; ++i) {
-              float2 v2 = __bfloat1622float2(vr[i]);
-              o[2 * i] = fmaf(pk, v2.x, o[2 * i]);
-              o[2 * i + 1] = fmaf(pk, v2.y, o[2 * i + 1]);
-            }
-          }
-        }
-        const int slot_end = slot0 + (sb + 1) * 16;
-        if (slot_end % C == 0) {
-          const int c = slot_end / C - 1;
-          if (c < n_ch) {
-            float val = csum > 0.f ? m + log2f(csum) : -CUDART_INF_F;
-            int64_t idx = ((((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi) *
-                               a.plan.max_chunks + c) * kRowsPerGroup + r;
-            a.clse[idx] = val;
-          }
-          csum = 0.f;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (row_ok) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    float* op = a.o_part + ((int64_t)item * kRowsPerGroup + r) * D;
-#pragma unroll
-    for (int d = 0; d < D; d += 4)
-      *reinterpret_cast<float4*>(op + d) =
-          make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
-    a.lse_part[(int64_t)item * kRowsPerGroup + r] =
-        l > 0.f ? m + log2f(l) : -CUDART_INF_F;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// combine: one warp per (sequence, kv head, row group, row).
+// combine: one warp per (sequence, kv head, row group, row).  The split
+// log2-sum-exps are read lane-parallel; split outputs are accumulated eight
+// splits at a time so that eight 16-byte loads per lane are in flight.
 template <int D>
 __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
   __shared__ Plan s_plan;
@@ -221,27 +54,51 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
   const int qh = h * G + grow % G;
   const int base = sq.item_base + (h * sq.rg + rgi) * sq.splits;
   const int ns = sq.splits;
+  const float* lp = a.lse_part + (int64_t)base * kRowsPerGroup + r;
 
   float mx = -CUDART_INF_F;
-  for (int s = lane; s < ns; s += 32)
-    mx = fmaxf(mx, a.lse_part[(int64_t)(base + s) * kRowsPerGroup + r]);
+  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * kRowsPerGroup));
   mx = warp_max(mx);
   float sum = 0.f;
-  for (int s = lane; s < ns; s += 32)
-    sum += exp2f(a.lse_part[(int64_t)(base + s) * kRowsPerGroup + r] - mx);
+  for (int s = lane; s < ns; s += 32) sum += exp2f(__ldg(lp + (int64_t)s * kRowsPerGroup) - mx);
   sum = warp_sum(sum);
   const float lse = mx + log2f(sum);
 
-  constexpr int E = D / 32;
+  constexpr int E = D / 32;   // floats per lane (4 or 2)
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = exp2f(a.lse_part[(int64_t)(base + s) * kRowsPerGroup + r] - lse);
-    if (w == 0.f) continue;
-    const float* op = a.o_part + ((int64_t)(base + s) * kRowsPerGroup + r) * D + lane * E;
+  const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
+  const int64_t sstride = (int64_t)kRowsPerGroup * D;
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    // weight of split s0 + lane, broadcast below
+    const float wl = (s0 + lane < ns)
+                         ? exp2f(__ldg(lp + (int64_t)(s0 + lane) * kRowsPerGroup) - lse) : 0.f;
+    const int cnt = min(32, ns - s0);
+    for (int k0 = 0; k0 < cnt; k0 += 8) {
+      float x[8][E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, op[e], acc[e]);
+      for (int k = 0; k < 8; ++k) {
+        if (k0 + k < cnt) {
+          const float* op = op0 + (int64_t)(s0 + k0 + k) * sstride;
+          if constexpr (E == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(op));
+            x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
+          } else {
+            const float2 v = __ldg(reinterpret_cast<const float2*>(op));
+            x[k][0] = v.x; x[k][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
+        if (k0 + k < cnt && w != 0.f) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
+        }
+      }
+    }
   }
   const int64_t obase = ((int64_t)node * a.num_q_heads + qh) * D + lane * E;
   if (a.out_f32) {
@@ -259,36 +116,43 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// finalize: one warp per (sequence, chunk).
+// finalize: one CTA per (chunk, sequence).  Warp w sums the rows of kv heads
+// / row groups w, w + 8, ...; each lane keeps eight loads of chunk mass and
+// eight of row log2-sum-exp in flight.
 __global__ void __launch_bounds__(256) chunk_finalize(VerifyKArgs a) {
-  __shared__ Plan s_plan;
+  __shared__ float s_part[8];
   const int b = blockIdx.y;
-  if (threadIdx.x < 32) {
-    Plan p = plan_find(a.plan, b, 0);
-    if (threadIdx.x == 0) s_plan = p;
-  }
-  __syncthreads();
-  const Plan p = s_plan;
-  if (p.b < 0) return;
-  const SeqPlan& sq = p.seq;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * 8 + warp;
+  const int c = blockIdx.x;
+  const SeqPlan sq = seq_sizes(a.plan, b, false);
   const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
   if (c >= n_ch) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float sum = 0.f;
-  for (int h = 0; h < a.plan.num_kv_heads; ++h) {
-    for (int rgi = 0; rgi < sq.rg; ++rgi) {
-      const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
-      const int64_t hb = ((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi;
-      const float* cl = a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup;
-      const float* rl = a.row_lse + hb * kRowsPerGroup;
-      for (int r = lane; r < rows_here; r += 32) sum += exp2f(cl[r] - rl[r]);
+  const int combos = a.plan.num_kv_heads * sq.rg;
+  for (int cb = warp; cb < combos; cb += 8) {
+    const int h = cb / sq.rg, rgi = cb % sq.rg;
+    const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
+    const int64_t hb = ((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi;
+    const float* cl = a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup;
+    const float* rl = a.row_lse + hb * kRowsPerGroup;
+    float v[8], w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int r = lane + 32 * k;
+      v[k] = r < rows_here ? __ldg(cl + r) : -CUDART_INF_F;
+      w[k] = r < rows_here ? __ldg(rl + r) : 0.f;
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sum += exp2f(v[k] - w[k]);
   }
   sum = warp_sum(sum);
-  if (lane == 0) {
+  if (lane == 0) s_part[warp] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += s_part[i];
     float* dst = a.scores + (int64_t)b * a.plan.max_chunks + c;
-    *dst = a.accumulate ? *dst + sum : sum;
+    *dst = a.accumulate ? *dst + t : t;
   }
 }
 
@@ -301,35 +165,16 @@ template <int D>
 static cudaError_t launch_d(const VerifyKArgs& k, const ds_verify_args& a,
                             const VerifyLayout& L, int batch, cudaStream_t stream,
                             cudaEvent_t ev0, cudaEvent_t ev1) {
-  const size_t smem = 2ull * kTileKeys * D * sizeof(__nv_bfloat16);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(verify_split_simt<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  static const bool simt = [] {
-    const char* v = getenv("DS_SPLIT_IMPL");
-    return v && v[0] == 's';
-  }();
   if (ev0) cudaEventRecord(ev0, stream);
-  cudaError_t e;
-  if (simt) {
-    verify_split_simt<D><<<L.max_items, 256, smem, stream>>>(k);
-    e = cudaGetLastError();
-  } else {
-    e = launch_split_tc(k, a, L, stream);
-  }
+  cudaError_t e = launch_split_tc(k, a, L, stream);
   if (e != cudaSuccess) return e;
   if (ev1) cudaEventRecord(ev1, stream);
   dim3 gc(batch * k.plan.num_kv_heads * L.rg_max, kRowsPerGroup / 8);
   verify_combine<D><<<gc, 256, 0, stream>>>(k);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 gf((k.plan.max_chunks + 7) / 8, batch);
   if (k.plan.max_chunks > 0) {
+    dim3 gf(k.plan.max_chunks, batch);
     chunk_finalize<<<gf, 256, 0, stream>>>(k);
     e = cudaGetLastError();
   }
