@@ -367,7 +367,7 @@ def run_ours(args, wl, rank, world, local_rank):
     alg_bytes = kvb + _q_bytes(wl, st)
     achieved = alg_bytes / (split_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "long_context_speculative_ds_gb300", "csrc",
-                       "verify_attn.cu")
+                       "verify_tc.cu")
     line = {
         "metric": METRIC, "value": round(us, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
