@@ -272,6 +272,40 @@ void ds_accept_args_default(ds_accept_args* args);
 ds_status ds_accept_workspace_size(const ds_accept_args* args, size_t* bytes);
 ds_status ds_accept(const ds_accept_args* args, void* stream);
 
+/* Tree acceptance without a caller-supplied workspace.  The method itself
+ * has no counterpart to this entry: it is ds_accept for callers that cannot
+ * hand out device memory where they call it (a plugin or host callback
+ * whose framework owns every allocation and gives it no allocator, or a
+ * serving loop that forbids allocation once warm).
+ *
+ * Same arguments, kernels and results as ds_accept, except that
+ * args->workspace must be NULL and args->workspace_bytes 0: the scratch
+ * (a status word and one 48-byte record per tree node) is a fixed array in
+ * device global memory inside the library, DS_ACCEPT_STATIC_MAX_NODES
+ * records long (about 193 KiB per device).  Nothing is allocated, on the
+ * device or through any library, by this call.
+ *
+ * Refused with DS_ERR_UNSUPPORTED: args->n_nodes > DS_ACCEPT_STATIC_MAX_NODES
+ * (use ds_accept).  Refused with DS_ERR_INVALID_ARG: a non-NULL workspace.
+ *
+ * Setup: the first call made while a given device is current looks up the
+ * array's address on that device (cudaGetSymbolAddress); make that first
+ * call before capturing `stream` into a graph.  Each call then enqueues, on
+ * `stream`, a zeroing of the status word (the one part of the scratch that
+ * must start at zero; the node records are written before they are read)
+ * and the acceptance kernels.
+ *
+ * flags_out: NULL to return as soon as the work is enqueued; otherwise the
+ * call synchronises `stream` and stores this call's device status bits
+ * (DS_DEV_BAD_TREE, DS_DEV_BAD_TOKEN; 0 = inputs valid) at *flags_out.
+ *
+ * One scratch per device: two calls whose work may overlap on the device
+ * (different streams, or different host threads, without ordering between
+ * them) race on it and give undefined results.  Serialise them. */
+#define DS_ACCEPT_STATIC_MAX_NODES 4096
+ds_status ds_accept_static(const ds_accept_args* args, uint32_t* flags_out,
+                           void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -77,7 +77,8 @@ EXPORTS = ("ds_last_error", "ds_abi_version", "ds_struct_size",
            "ds_verify_args_default", "ds_verify_attn_workspace_size",
            "ds_verify_attn", "ds_gather_args_default",
            "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
-           "ds_accept_args_default", "ds_accept_workspace_size", "ds_accept")
+           "ds_accept_args_default", "ds_accept_workspace_size", "ds_accept",
+           "ds_accept_static")
 
 
 def lib_path() -> str:
@@ -102,7 +103,7 @@ def load(path: Optional[str] = None) -> C.CDLL:
     for name in ("ds_workspace_init", "ds_device_status",
                  "ds_verify_attn_workspace_size", "ds_verify_attn",
                  "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
-                 "ds_accept_workspace_size", "ds_accept"):
+                 "ds_accept_workspace_size", "ds_accept", "ds_accept_static"):
         getattr(lib, name).restype = C.c_int
     for which, cls in enumerate((VerifyArgs, GatherArgs, AcceptArgs)):
         got = lib.ds_struct_size(which)
@@ -258,6 +259,17 @@ def ds_accept_workspace_size(args: AcceptArgs) -> int:
 
 def ds_accept(args: AcceptArgs, stream=None):
     _check(load().ds_accept(C.byref(args), _stream(stream)))
+
+
+def ds_accept_static(args: AcceptArgs, stream=None, read_flags: bool = True):
+    """ds_accept over the library's own scratch (args.workspace must be
+    unset).  With read_flags the call waits for the stream and returns the
+    device status bits of this call; otherwise it returns None at once."""
+    flags = C.c_uint32(0)
+    _check(load().ds_accept_static(C.byref(args),
+                                   C.byref(flags) if read_flags else None,
+                                   _stream(stream)))
+    return flags.value if read_flags else None
 
 
 def ds_workspace_init(workspace: torch.Tensor, stream=None):

@@ -123,6 +123,11 @@ AcceptLayout accept_layout(const ds_accept_args& a) {
   return L;
 }
 
+ds_status set_last_error(ds_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+
 }  // namespace ds
 
 extern "C" {
