@@ -212,7 +212,9 @@ accept_node_pass(AcceptKArgs a) {
   const int b = seq_of(a.offsets, a.batch, node);
   const int n0 = __ldg(a.offsets + b);
   int T = __ldg(a.offsets + b + 1) - n0;
-  if (T > DS_MAX_TREE_NODES || T < 0) T = 0;
+  // a malformed tree (flagged by the walk) gets no children, so no parent
+  // read leaves the node arrays
+  if (T > DS_MAX_TREE_NODES || T < 0 || n0 < 0 || n0 + T > a.n_nodes) T = 0;
   if (threadIdx.x == 0) {
     int nch = 0;
     const int i = node - n0;

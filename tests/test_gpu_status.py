@@ -57,3 +57,16 @@ def test_bad_token_flag():
     step.accept()
     torch.cuda.synchronize()
     assert B.ds_device_status(step.ws_accept) & B.DS_DEV_BAD_TOKEN
+
+
+def test_bad_tree_offsets_flag_in_accept():
+    """An offset past the node arrays: the walk flags the sequence and gives
+    it n = 0, bonus -1; the node pass gives it no children, so no parent or
+    token read leaves the arrays."""
+    wl, st, inp = _case()
+    step = H.make_step(wl, inp, "reject")
+    inp.tree_offsets[2] = st.n_nodes + 5
+    step.accept()
+    torch.cuda.synchronize()
+    assert B.ds_device_status(step.ws_accept) & B.DS_DEV_BAD_TREE
+    assert int(step.out_n[1]) == 0 and int(step.out_bonus[1]) == -1
