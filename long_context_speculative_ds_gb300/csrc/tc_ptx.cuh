@@ -203,6 +203,12 @@ DS_DEV uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// max of three (the three-operand form of max.f32)
+DS_DEV float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 DS_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

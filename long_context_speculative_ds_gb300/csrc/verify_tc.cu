@@ -8,8 +8,8 @@
 //               box per (page, 64-column half); the one or two tiles that
 //               hold tree slots or the end of the sequence are copied with
 //               plain loads so that slots past the sequence end read as zero.
-//   warp 1      tensor-memory allocator and MMA issuer (one thread).
-//   warps 2-3   idle after set-up.
+//   warp 1      tensor-memory allocator.
+//   warps 2, 3  MMA issuers of softmax groups 0 and 1 (one thread each).
 //   warps 4-7   softmax group 0, warps 8-11 softmax group 1 (each a whole
 //               warpgroup): one query row per thread, tensor-memory lane
 //               32 * (warp % 4) + lane.
@@ -18,13 +18,17 @@
 // rows group g takes rows 128g..128g+127 of every tile ("row mode"); with at
 // most 128 rows both groups use the same rows and take alternate tiles, and
 // their partial results are merged at the end ("key mode").  Tensor memory,
-// 256 columns per group: S (128 columns) and O (128 columns).  Per tile the
-// MMA thread issues S = Q K^T (one M128 N128 chain); the group turns S into
-// bf16 P in two 64-key halves, P of half h over columns 32h..32h+31, and
-// signals each half separately, so O += P V of the first half runs while the
-// group works on the second; after the second half's P V the MMA thread
-// issues the group's next S.  Two groups keep the tensor pipe busy while
-// either one computes exponentials.
+// 256 columns per group: two 64-column half slots and O (128 columns).
+// Half slot h holds S = Q K^T of keys 64h..64h+63 of the group's tile (one
+// M128 N64 chain), which the group turns into bf16 P in place and signals;
+// the group's issuer then issues O += P V for that half and, into the same
+// slot (the pipe runs in order), S of the same half of the group's next
+// tile.  So each half's S is ready long before the group gets to it, and
+// the two groups keep the tensor pipe busy while either computes
+// exponentials.  A thread that has issued tcgen05.mma pays for its own
+// next shared-memory access (a barrier test included) with the time its
+// queued MMAs take to drain; with one issuer per group, each issuer waits
+// only for its own group's P, by which time its MMAs have completed.
 //
 // Softmax works in log2 units with lazy rescaling: the running maximum only
 // moves (and O is rescaled, after the previous P V has completed) when a
@@ -57,18 +61,19 @@ constexpr int kTmemCols = 512;
 
 enum Bar {
   kQFull = 0,
-  kKFull = 1,      // 3 slots
-  kKEmpty = 4,     // 3 slots
-  kVFull = 7,      // 3 slots
-  kVEmpty = 10,    // 3 slots
-  kSFull = 13,     // [group]: S of the group's next tile is ready
-  kPFull = 15,     // [group][half]: P of one 64-key half is ready; one
+  kKFull = 1,      // [group][slot] in key mode, [0][slot] in row mode
+  kKEmpty = 7,     // 3 slots
+  kVFull = 10,     // [group][slot] in key mode, [0][slot] in row mode
+  kVEmpty = 16,    // 3 slots
+  kSFull = 19,     // [group][half]: S of the group's next 64-key half is
+                   // ready in that half's tensor-memory slot
+  kPFull = 23,     // [group][half]: P of one 64-key half is ready; one
                    // barrier per half, so that a group can never complete
                    // two phases of one barrier before the MMA thread has
                    // seen the first
-  kORdy = 19,      // [group]: one completion per issued P V
-  kOFinal = 21,
-  kNumBars = 22
+  kORdy = 27,      // [group]: one completion per issued P V
+  kOFinal = 29,    // [group]: all of the group's MMAs have completed
+  kNumBars = 31
 };
 
 struct Ctrl {
@@ -78,7 +83,7 @@ struct Ctrl {
   Plan plan;
   int32_t parents[DS_MAX_TREE_NODES];
   uint64_t anc[DS_MAX_TREE_NODES];
-  uint32_t where[4];   // last wait site of loader, MMA, softmax groups 0 and 1
+  uint32_t where[5];   // last wait site of loader, issuer 0, softmax 0, softmax 1, issuer 1
 };
 
 template <int D>
@@ -87,6 +92,7 @@ struct Cfg {
   static constexpr int NH = D / 64;        // 128-byte column halves
   // Q (2 tiles) + K ring (2 slots) + V ring (3 slots) + control block
   static constexpr size_t smem = 7 * TB + sizeof(Ctrl) + 1024;
+  static_assert(smem <= 232448, "dynamic shared memory above the 227 KB a block can have");
 };
 
 // One 64-key unit of one softmax thread (one query row): loads the row's 64
@@ -102,7 +108,7 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t tP, const uint32_t vw
                          const uint32_t vw1,
                          const uint32_t cw0, const uint32_t cw1, const float c2, const bool first,
                          float& m2, float& l, float& cs, float& alpha, bool& rescale,
-                         const int tile_slot0, const int kbase, const int C, const int n_ch,
+                         const int tile_slot0, const int kbase, const int cshift, const int n_ch,
                          const bool row_ok, float* __restrict__ clse_row) {
   using namespace ptx;
   float s[64];
@@ -125,16 +131,16 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t tP, const uint32_t vw
       if (!((vw1 >> c) & 1u)) s[32 + c] = -CUDART_INF_F;
     }
   }
-  // row maximum: four independent chains of 16
+  // row maximum: three-input max, four independent chains of 16
   float mx4[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float m = s[16 * k];
+    float m = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
 #pragma unroll
-    for (int i = 1; i < 16; ++i) m = fmaxf(m, s[16 * k + i]);
-    mx4[k] = m;
+    for (int i = 3; i < 15; i += 2) m = fmax3(m, s[16 * k + i], s[16 * k + i + 1]);
+    mx4[k] = fmaxf(m, s[16 * k + 15]);
   }
-  const float mx2 = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+  const float mx2 = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c2;
   alpha = 1.f;
   rescale = false;
   if (first) {
@@ -195,14 +201,14 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t tP, const uint32_t vw
   l = l * alpha + (tsum + ((cg[0] + cg[1]) + (cg[2] + cg[3])));
   // chunk log2-mass at chunk boundaries (C/16 sixteen-column groups a chunk)
   {
-    const int per_mask = (C >> 4) - 1;
+    const int per_mask = (1 << (cshift - 4)) - 1;
     cs *= alpha;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       cs += cg[k];
       const int kg = kbase + k;          // 16-column group index in the tile
       if (((kg + 1) & per_mask) == 0) {
-        const int cidx = (tile_slot0 + kg * 16) / C;
+        const int cidx = (tile_slot0 + kg * 16) >> cshift;
         if (row_ok && cidx < n_ch)
           clse_row[(int64_t)cidx * kRowsPerGroup] = cs > 0.f ? mb + __log2f(cs) : -CUDART_INF_F;
         cs = 0.f;
@@ -317,22 +323,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) ctrl->plan = p;
   } else if (warp == 1 && lane == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < 6; ++s) {
       mbar_init(bar(kKFull + s), 1);
-      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kVFull + s), 1);
     }
     for (int s = 0; s < 3; ++s) {
-      mbar_init(bar(kVFull + s), 1);
-      mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kKEmpty + s), 2);   // one commit per group (two in key mode)
+      mbar_init(bar(kVEmpty + s), 2);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kORdy + s), 1);
-      mbar_init(bar(kSFull + s), 1);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kORdy + s), 1);
+    for (int s = 0; s < 4; ++s) mbar_init(bar(kSFull + s), 1);
     for (int s = 0; s < 4; ++s) mbar_init(bar(kPFull + s), 128);
-    mbar_init(bar(kOFinal), 1);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kOFinal + s), 1);
     ctrl->abort = 0;
-    for (int i = 0; i < 4; ++i) ctrl->where[i] = 0;
+    for (int i = 0; i < 5; ++i) ctrl->where[i] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -415,6 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int kslots = row_mode ? 2 : 3;
   const int klead = row_mode ? 1 : 2;
+  // Full barrier of K (is_v 0) or V (is_v 1) tile n and the parity of its
+  // phase.  In key mode the groups take alternate tiles and share three-slot
+  // rings, so each slot has one full barrier per group: a group then waits
+  // on every phase of its barriers in order and never tests a barrier two
+  // phases short of the tile it wants (the parity test would pass on the
+  // wrong phase).
+  auto full_bar = [&](int is_v, int n) -> int {
+    const int base = is_v ? kVFull : kKFull;
+    if (row_mode) return base + (is_v ? n % 3 : n % kslots);
+    return base + n % 3 + 3 * (n & 1);
+  };
+  auto full_par = [&](int is_v, int n) -> uint32_t {
+    if (row_mode) return (uint32_t)((is_v ? n / 3 : n / kslots) & 1);
+    return (uint32_t)((n / 6) & 1);
+  };
   auto kslot_addr = [&](int s) -> uint32_t { return s < 2 ? sK + s * TB : sQ + TB; };
   auto vslot_addr = [&](int s) -> uint32_t { return sV + s * TB; };
   // tiles of group g: row mode every tile, key mode every other tile
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nslots = is_v ? 3 : kslots;
         const int slot = n % nslots;
         const int use = n / nslots;
-        const uint32_t full = bar((is_v ? kVFull : kKFull) + slot);
+        const uint32_t full = bar(full_bar(is_v, n));
         const uint32_t empty = bar((is_v ? kVEmpty : kKEmpty) + slot);
         const uint32_t dst = is_v ? vslot_addr(slot) : kslot_addr(slot);
         const int slot0 = t * kTileKeys;
@@ -553,103 +572,114 @@ __global__ void __launch_bounds__(kThreads, 1)
       // copies still in flight must land before the CTA can exit
       if (!ok && lane == 0) {
         for (int n = max(0, nk - kslots); n < nk; ++n)
-          drain_wait(bar(kKFull + n % kslots), (n / kslots) & 1);
+          drain_wait(bar(full_bar(0, n)), full_par(0, n));
         for (int n = max(0, nv - 3); n < nv; ++n)
-          drain_wait(bar(kVFull + n % 3), (n / 3) & 1);
+          drain_wait(bar(full_bar(1, n)), full_par(1, n));
       }
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA
+    } else if (warp == 2 || warp == 3) {
+      // ------------------------------------------------------ MMA issuers
+      // One issuing thread per softmax group (warp 2: group 0, warp 3:
+      // group 1).  A thread that has issued tcgen05.mma pays for any later
+      // shared-memory access of its own with the time its queued MMAs need
+      // to drain, so each group's MMAs come from a thread that only waits
+      // on that group's P, at a point where its own MMAs have long
+      // completed; the two groups never hold each other up.
+      const int g = warp - 2;
       if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
         // Descriptor bases computed once; each MMA only adds a compile-time
         // offset to the 14-bit start-address field (addresses stay below
         // 256 KB, so the add never carries into the neighbouring fields).
         const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);
-        const uint64_t qdg = row_mode ? qd0 + (TB >> 4) : qd0;   // Q of group 1
+        const uint64_t qb = (row_mode && g == 1) ? qd0 + (TB >> 4) : qd0;   // this group's Q
         const uint64_t kd0 = sdesc_sw128(sK, 16, 1024);
         const uint64_t kd2 = sdesc_sw128(sQ + TB, 16, 1024);      // K slot 2 (key mode)
         const uint64_t vd0 = sdesc_sw128(sV, kHalfBytes, 1024);
+        const uint32_t tG = tmem + (uint32_t)(256 * g);
+        // users of each K and V tile: both groups in row mode, one in key
+        // mode (which then releases the slot with two commits)
+        const int rel = row_mode ? 1 : 2;
         auto kslot_of = [&](int t) { return row_mode ? (t & 1) : (t % 3); };
-        auto kuse_of = [&](int t) { return row_mode ? (t >> 1) : (t / 3); };
-        // S[g] at column 256 g (128 columns), O[g] at 256 g + 128
-        auto qk = [&](int g, int t) {
+        // half slot h (64 columns at tG + 64 h) holds S, then P in place,
+        // of keys 64 h .. 64 h + 63 of the group's current tile; O at
+        // tG + 128.  S of a half slot's next tile is issued right after the
+        // P V that reads the slot (the pipe runs in order), so the group's
+        // next half is ready while it still works on the other half.
+        auto qk = [&](int t, int h) {
           const int ks = kslot_of(t);
-          const uint64_t kb = ks < 2 ? kd0 + (uint64_t)(ks * (TB >> 4)) : kd2;
-          const uint64_t qb = g ? qdg : qd0;
-          const uint32_t d = tmem + (uint32_t)(256 * g);
+          const uint64_t kb = (ks < 2 ? kd0 + (uint64_t)(ks * (TB >> 4)) : kd2) +
+                              (uint64_t)(h * (kUnitRowOff >> 4));
+          const uint32_t d = tG + (uint32_t)(64 * h);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
             mma_ss(d, qb + off, kb + off, idesc_qk, kk > 0);
           }
         };
-        // O[g] += P(half hb) V(keys 64 hb .. 64 hb + 63)
-        auto pv = [&](int g, int t, int hb, bool acc) {
-          const uint64_t vb = vd0 + (uint64_t)((t % 3) * (TB >> 4) + hb * (kUnitRowOff >> 4));
-          const uint32_t d = tmem + (uint32_t)(256 * g + 128);
-          const uint32_t pa = tmem + (uint32_t)(256 * g + 32 * hb);
+        // O += P(half h) V(keys 64 h .. 64 h + 63)
+        auto pv = [&](int t, int h, bool acc) {
+          const uint64_t vb = vd0 + (uint64_t)((t % 3) * (TB >> 4) + h * (kUnitRowOff >> 4));
+          const uint32_t pa = tG + (uint32_t)(64 * h);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(d, pa + kk * 8, vb + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+            mma_ts(tG + 128, pa + kk * 8, vb + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                    (acc || kk > 0) ? 1u : 0u);
         };
-        auto wait_k = [&](int t) {
-          ctrl->where[1] = 20000 + kKFull * 100 + t;
-          return mbar_wait(bar(kKFull + kslot_of(t)), kuse_of(t) & 1, abort_flag, diag,
-                           20000 + kKFull * 100 + t);
+        const int wi = g == 0 ? 1 : 4;   // this issuer's slot in ctrl->where
+        auto wait = [&](int b, uint32_t par, uint32_t tag) {
+          ctrl->where[wi] = tag;
+          return mbar_wait(bar(b), par, abort_flag, diag, tag);
         };
-        const int ng = row_mode ? 2 : 1;   // groups that use each tile
-        ctrl->where[1] = 20000 + kQFull * 100;
-        bool ok = mbar_wait(bar(kQFull), 0, abort_flag, diag, 20000 + kQFull * 100);
-        // prologue: S of each group's first tile
-        for (int g = 0; ok && g < 2; ++g) {
-          if (ntiles(g) == 0) continue;
+        auto wait_k = [&](int t) {
+          return wait(full_bar(0, t), full_par(0, t), 20000 + kKFull * 100 + t);
+        };
+        auto wait_v = [&](int n) {
+          return wait(full_bar(1, n), full_par(1, n), 20000 + kVFull * 100 + n);
+        };
+        const int my_nt = ntiles(g);
+        bool ok = wait(kQFull, 0, 20000 + kQFull * 100);
+        // prologue: S of both halves of the group's first tile
+        if (ok && my_nt > 0) {
           const int t = tile_of(g, 0);
-          if (row_mode ? g == 0 : true) {
-            if (!(ok = wait_k(t))) break;
+          if ((ok = wait_k(t))) {
             tc_fence_after();
+            for (int h = 0; h < 2; ++h) {
+              qk(t, h);
+              mma_commit(bar(kSFull + 2 * g + h));
+            }
+            for (int r = 0; r < rel; ++r) mma_commit(bar(kKEmpty + kslot_of(t)));
           }
-          qk(g, t);
-          mma_commit(bar(kSFull + g));
-          if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + kslot_of(t)));
         }
-        for (int n = 0; ok && n < nt; ++n) {
-          ctrl->where[1] = 20000 + kVFull * 100 + n;
-          if (!(ok = mbar_wait(bar(kVFull + n % 3), (n / 3) & 1, abort_flag, diag,
-                               20000 + kVFull * 100 + n)))
-            break;
-          for (int gi = 0; ok && gi < ng; ++gi) {
-            const int g = row_mode ? gi : (n & 1);
-            const int j = row_mode ? n : (n - g) / 2;
-            for (int hb = 0; hb < 2; ++hb) {
-              ctrl->where[1] = 20000 + (kPFull + 2 * g + hb) * 100 + 2 * j + hb;
-              if (!(ok = mbar_wait(bar(kPFull + 2 * g + hb), j & 1, abort_flag, diag,
-                                   20000 + (kPFull + 2 * g + hb) * 100 + 2 * j + hb)))
-                break;
-              tc_fence_after();
-              pv(g, n, hb, j > 0 || hb > 0);
-              mma_commit(bar(kORdy + g));
+        for (int j = 0; ok && j < my_nt; ++j) {
+          const int n = tile_of(g, j);
+          const bool more = j + 1 < my_nt;
+          const int tn = more ? tile_of(g, j + 1) : 0;
+          for (int h = 0; h < 2; ++h) {
+            if (!(ok = wait(kPFull + 2 * g + h, j & 1,
+                            20000 + (kPFull + 2 * g + h) * 100 + 2 * j + h)))
+              break;
+            if (h == 0) {
+              if (!(ok = wait_v(n))) break;
+              if (more && !(ok = wait_k(tn))) break;
             }
-            if (!ok) break;
-            if (j + 1 < ntiles(g)) {
-              // S is free once this tile's P V has been issued (in-order pipe)
-              const int tn = tile_of(g, j + 1);
-              if (row_mode ? g == 0 : true) {
-                if (!(ok = wait_k(tn))) break;
-                tc_fence_after();
-              }
-              qk(g, tn);
-              mma_commit(bar(kSFull + g));
-              if (row_mode ? g == 1 : true) mma_commit(bar(kKEmpty + kslot_of(tn)));
+            tc_fence_after();
+            pv(n, h, j > 0 || h > 0);
+            mma_commit(bar(kORdy + g));
+            if (more) {
+              qk(tn, h);
+              mma_commit(bar(kSFull + 2 * g + h));
+              if (h == 1)
+                for (int r = 0; r < rel; ++r) mma_commit(bar(kKEmpty + kslot_of(tn)));
             }
+            if (h == 1)
+              for (int r = 0; r < rel; ++r) mma_commit(bar(kVEmpty + n % 3));
           }
-          if (ok) mma_commit(bar(kVEmpty + n % 3));
         }
         // all issued MMAs complete -> epilogue (also on the abort path, so
         // that nothing is in flight when tensor memory is freed)
-        if (ok) ctrl->where[1] = 29999;
-        mma_commit(bar(kOFinal));
+        if (ok) ctrl->where[wi] = 29999;
+        mma_commit(bar(kOFinal + g));
       }
     }
   } else {
@@ -668,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tO = tG + 128;
       const float c2 = a.scale_log2;
       const int C = a.plan.chunk_size;
+      const int cshift = __ffs(C) - 1;               // C is a power of two >= 16
       const int n_ch = (L + C - 1) / C;
       float* clse_row = a.clse +
                         (((int64_t)p.b * a.plan.num_kv_heads + kvh) * a.plan.rg_max + rgi) *
@@ -679,21 +710,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < my_nt; ++j) {
         const int n = tile_of(g, j);
         const int tile_slot0 = (t0 + n) * kTileKeys;
-        if (lrow == 0) ctrl->where[2 + g] = 30000 + (kSFull + g) * 100 + j;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + g), j & 1, abort_flag, diag,
-                                               30000 + (kSFull + g) * 100 + j));
-        if (!ok) break;
-        tc_fence_after();
         for (int hb = 0; hb < 2; ++hb) {
           const int u = 2 * j + hb;
+          if (lrow == 0) ctrl->where[2 + g] = 30000 + (kSFull + 2 * g + hb) * 100 + j;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull + 2 * g + hb), j & 1, abort_flag,
+                                                 diag, 30000 + (kSFull + 2 * g + hb) * 100 + j));
+          if (!ok) break;
+          tc_fence_after();
           const uint32_t tS = tG + 64 * hb;     // scores of keys 64 hb .. 64 hb + 63
-          const uint32_t tP = tG + 32 * hb;     // their P (bf16 pairs)
+          const uint32_t tP = tS;               // their P (bf16 pairs), in place
           const int unit_slot0 = tile_slot0 + 64 * hb;
           float alpha;
           bool rescale;
           if (unit_slot0 + 64 <= L) {
             softmax_unit<false>(tS, tP, ~0u, ~0u, ~0u, ~0u, c2, u == 0, m2, l, cs, alpha,
-                                rescale, tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
+                                rescale, tile_slot0, 4 * hb, cshift, n_ch, row_ok, clse_row);
           } else {
             // column c is visible iff c < L - unit_slot0 (context) or it is
             // tree slot i = c - (L - unit_slot0) with bit i of the row's
@@ -705,17 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t vis = ctx | tr;
             softmax_unit<true>(tS, tP, (uint32_t)vis, (uint32_t)(vis >> 32), (uint32_t)ctx,
                                (uint32_t)(ctx >> 32), c2, u == 0, m2, l, cs, alpha, rescale,
-                               tile_slot0, 4 * hb, C, n_ch, row_ok, clse_row);
+                               tile_slot0, 4 * hb, cshift, n_ch, row_ok, clse_row);
           }
           if (rescale) {
-            // O must hold the sum over all earlier halves: before the first
-            // half that is guaranteed (this S was issued after the previous
-            // P V); before the second half wait for the first half's P V
-            if (hb == 1) {
-              if (lrow == 0) ctrl->where[2 + g] = 30000 + (kORdy + g) * 100 + u;
-              ok = __all_sync(0xffffffffu, mbar_wait(bar(kORdy + g), (u - 1) & 1, abort_flag,
-                                                     diag, 30000 + (kORdy + g) * 100 + u));
-            }
+            // O must hold the sum over all earlier halves: wait for the
+            // previous half's P V (the one before it completed before this
+            // half's S, which was issued after it)
+            if (lrow == 0) ctrl->where[2 + g] = 30000 + (kORdy + g) * 100 + u;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kORdy + g), (u - 1) & 1, abort_flag,
+                                                   diag, 30000 + (kORdy + g) * 100 + u));
             if (ok) {
               tc_fence_after();
 #pragma unroll 1
@@ -737,10 +766,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ------------------------------------------------------------ epilogue
-      if (lrow == 0) ctrl->where[2 + g] = 30000 + kOFinal * 100;
+      // key mode merges the groups through shared memory that the V ring
+      // uses, so there both groups' MMAs must be complete (and with them
+      // every V load); row mode needs only the group's own
+      if (lrow == 0) ctrl->where[2 + g] = 30000 + (kOFinal + g) * 100;
       if (ok)
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(kOFinal), 0, abort_flag, diag, 30000 + kOFinal * 100));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFinal + g), 0, abort_flag, diag,
+                                               30000 + (kOFinal + g) * 100));
+      if (ok && !row_mode)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFinal + 1 - g), 0, abort_flag, diag,
+                                               30000 + (kOFinal + 1 - g) * 100));
       else __syncwarp();
       if (ok) tc_fence_after();
       const int nt1 = row_mode ? 0 : ntiles(1);    // tiles of group 1 in key mode
@@ -757,10 +792,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag && threadIdx.x == 0) {
     flag(a.plan.status, DS_DEV_TIMEOUT);
     if (diag[1] == blockIdx.x)
-      for (int i = 0; i < 4; ++i) diag[2 + i] = ctrl->where[i];
+      for (int i = 0; i < 5; ++i) diag[2 + i] = ctrl->where[i];
   }
   if (warp == 1) {
-    if (active && nt > 0 && lane == 0) drain_wait(bar(kOFinal), 0);
+    if (active && nt > 0 && lane == 0) {
+      drain_wait(bar(kOFinal), 0);
+      drain_wait(bar(kOFinal + 1), 0);
+    }
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
