@@ -659,14 +659,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait(kPFull + 2 * g + h, j & 1,
                             20000 + (kPFull + 2 * g + h) * 100 + 2 * j + h)))
               break;
-            if (h == 0) {
-              if (!(ok = wait_v(n))) break;
-              if (more && !(ok = wait_k(tn))) break;
-            }
+            if (h == 0 && !(ok = wait_v(n))) break;
             tc_fence_after();
             pv(n, h, j > 0 || h > 0);
             mma_commit(bar(kORdy + g));
             if (more) {
+              // the next tile's K is waited for only now, so that a late K
+              // copy does not hold back this half's P V
+              if (h == 0) {
+                if (!(ok = wait_k(tn))) break;
+                tc_fence_after();
+              }
               qk(tn, h);
               mma_commit(bar(kSFull + 2 * g + h));
               if (h == 1)
