@@ -29,6 +29,9 @@ step, with no blocking, fusion or reordering:
   * greedy_accept: accept-if-equal against the target argmax, walking the tree
     from the root (vllm.cpp docs "Speculative decoding", section "MTP":
     "greedy decoding plus accept-if-equal rejection").
+  * kv_commit: after acceptance the accepted path's tree K/V move into the
+    consecutive slots after the root and the length grows by 1 + n; the
+    stale tail is excluded by the length (adaptive-specdec README, "Layout").
   * rejection_accept: accept x ~ q with probability min(1, p(x)/q(x)); on
     rejection continue from the residual norm(max(0, p - q)) (adaptive-specdec
     README, "Correctness first" and "The controller"; Leviathan et al. 2023),
@@ -224,6 +227,59 @@ def gather_compact(src_k_bits, src_v_bits, page_table, ctx_lens, scores,
                 out_v[b, i] = src_v_bits[page, :, off]
     return dict(chunk_ids=chunk_ids, positions=positions, out_len=out_len,
                 out_k=out_k, out_v=out_v)
+
+
+# --------------------------------------------------------------------------
+# post-accept KV commit
+
+def kv_commit(k_bits, v_bits, page_table, ctx_lens, tree_offsets, path,
+              n_accepted, page_size: int, layout: str = "NHD"):
+    """Commit the accepted path of every sequence into its context, for one
+    layer's paged cache (raw bf16 bit patterns, any integer dtype).
+
+    The tree's K/V sit at slots L..L+T-1 in node order (node 0, the root, is
+    the last committed token and already sits at slot L).  The accepted nodes
+    c_1 < ... < c_n (path[b, :n]) move to the consecutive slots L+1..L+n and
+    the context length becomes L + 1 + n; the stale slots beyond it are simply
+    excluded by the length (adaptive-specdec README, "Layout": one buffer per
+    layer, a per-row lengths vector, writes scattered to each row's own
+    offset, rollback by length).  Sequences without a tree keep L.
+
+    Returns (k_out, v_out, new_lens) with the inputs left untouched."""
+    k_out = np.array(k_bits, copy=True)
+    v_out = np.array(v_bits, copy=True)
+    B = len(ctx_lens)
+    new_lens = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        L = int(ctx_lens[b])
+        T = int(tree_offsets[b + 1]) - int(tree_offsets[b])
+        if T == 0:
+            new_lens[b] = L
+            continue
+        n = int(n_accepted[b])
+        nodes = [int(x) for x in path[b][:n]]
+        if not (0 <= n <= T - 1) or any(not (0 < c < T) for c in nodes) or \
+                any(nodes[i] >= nodes[i + 1] for i in range(n - 1)):
+            raise ValueError(f"sequence {b}: path {nodes} is not increasing in (0, {T})")
+        # read every source row before writing any destination: a destination
+        # slot L+i can be the source slot of an earlier path entry
+        def slot(t):
+            return int(page_table[b][t // page_size]), t % page_size
+        rows_k, rows_v = [], []
+        for c in nodes:
+            pg, off = slot(L + c)
+            if layout == "NHD":
+                rows_k.append(np.array(k_bits[pg, off])); rows_v.append(np.array(v_bits[pg, off]))
+            else:
+                rows_k.append(np.array(k_bits[pg, :, off])); rows_v.append(np.array(v_bits[pg, :, off]))
+        for i, (rk, rv) in enumerate(zip(rows_k, rows_v), start=1):
+            pg, off = slot(L + i)
+            if layout == "NHD":
+                k_out[pg, off] = rk; v_out[pg, off] = rv
+            else:
+                k_out[pg, :, off] = rk; v_out[pg, :, off] = rv
+        new_lens[b] = L + 1 + n
+    return k_out, v_out, new_lens
 
 
 # --------------------------------------------------------------------------
