@@ -304,7 +304,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      draft_tokens=acc.draft_tokens, uniforms=acc.uniforms)
     step = VerifyStep(inp, chunk_size=wl.chunk_size, top_k=wl.top_k,
                       window=wl.window, accept_mode=mode,
-                      kv_layout=args.kv_layout)
+                      kv_layout=args.kv_layout, with_commit=True)
     # per-layer events around the split-pass kernel
     n_ev = args.steps * wl.layers
     evs = [(torch.cuda.Event(enable_timing=True),
@@ -344,6 +344,7 @@ def run_ours(args, wl, rank, world, local_rank):
             binding.ds_verify_attn(prof_args[s * wl.layers + l])
         step.gather()
         step.accept()
+        step.commit()
     e1.record()
     torch.cuda.synchronize()
     barrier()
@@ -352,6 +353,43 @@ def run_ours(args, wl, rank, world, local_rank):
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if world > 1:
         ms = max_over_ranks(ms, dev)
+
+    # the post-accept commit alone, on each tree's deepest root-to-leaf path
+    # (the longest accepted path the tree allows): it moves n rows per
+    # sequence, K and V, in every layer (read + write)
+    deep, n_acc = [], []
+    for b in range(wl.batch):
+        n0 = st.tree_offsets[b]
+        par = st.parents[n0:n0 + st.tree_sizes[b]]
+        depth = [0] * len(par)
+        for j in range(1, len(par)):
+            depth[j] = depth[par[j]] + 1
+        leaf = max(range(len(par)), key=lambda j: (depth[j], -j)) if par else 0
+        chain = []
+        while par and leaf > 0:
+            chain.append(leaf)
+            leaf = par[leaf]
+        chain.reverse()
+        deep.append(chain + [-1] * (binding.DS_MAX_TREE_NODES - len(chain)))
+        n_acc.append(len(chain))
+    c_new = torch.empty(wl.batch, **i32)
+    c_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    c_args = binding.commit_args(inp.k_cache, inp.v_cache, inp.page_table, inp.ctx_lens,
+                                 inp.tree_offsets, torch.tensor(deep, **i32),
+                                 torch.tensor(n_acc, **i32), new_ctx_lens=c_new,
+                                 workspace=c_ws, kv_layout=args.kv_layout)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    reps = 20
+    binding.ds_kv_commit(c_args)
+    c0.record()
+    for _ in range(reps):
+        binding.ds_kv_commit(c_args)
+    c1.record()
+    torch.cuda.synchronize()
+    assert binding.ds_device_status(c_ws) == 0
+    commit_us = c0.elapsed_time(c1) * 1e3 / reps
+    commit_bytes = sum(n_acc) * wl.num_kv_heads * wl.head_dim * 2 * 2 * 2 * wl.layers
 
     # end to end: pinned host inputs in, results out, every step
     e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else \
@@ -390,6 +428,10 @@ def run_ours(args, wl, rank, world, local_rank):
                 "note": "committed and tree K/V stay resident (model state);"
                         " per-step Q, tree, page table, logits, uniforms in,"
                         " path/bonus/chunk ids out"},
+        "kv_commit": {"us": round(commit_us, 2), "accepted": n_acc,
+                      "algorithmic_bytes": commit_bytes,
+                      "gbs": round(commit_bytes / (commit_us * 1e-6) / 1e9, 1)
+                      if commit_us > 0 else None},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
     }

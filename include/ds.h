@@ -11,7 +11,9 @@
  *   ds_chunk_topk_gather  top-k chunks by salience plus a recent window,
  *                         gathered into a compact contiguous cache;
  *   ds_accept             the accepted path: greedy accept-if-equal or exact
- *                         tree rejection sampling with supplied uniforms.
+ *                         tree rejection sampling with supplied uniforms;
+ *   ds_kv_commit          the accepted path's tree K/V moved behind the root
+ *                         in every layer, and the new context lengths.
  *
  * Conventions (all entry points):
  *   - Every pointer named in an args struct is a DEVICE pointer unless its
@@ -80,7 +82,7 @@ const char* ds_last_error(void);
 int32_t ds_abi_version(void);
 
 /* sizeof() of each args struct as compiled into the library: 0 verify,
- * 1 gather, 2 accept; -1 for anything else.  Bindings compare these with
+ * 1 gather, 2 accept, 3 commit; -1 for anything else.  Bindings compare these with
  * their own struct layouts before the first call. */
 int64_t ds_struct_size(int32_t which);
 
@@ -305,6 +307,54 @@ ds_status ds_accept(const ds_accept_args* args, void* stream);
 #define DS_ACCEPT_STATIC_MAX_NODES 4096
 ds_status ds_accept_static(const ds_accept_args* args, uint32_t* flags_out,
                            void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * Post-accept KV commit (adaptive-specdec README, "Layout": one cache buffer
+ * per layer, a per-sequence lengths vector, writes scattered to each row's
+ * own offset, rollback by length).
+ *
+ * For every sequence b with a tree (T = tree_offsets[b+1] - tree_offsets[b]
+ * >= 1) and L = ctx_lens[b]: the root's K/V (node 0) already sits at slot L;
+ * the accepted nodes c_1 < ... < c_n (path[b, 0..n-1], n = n_accepted[b], as
+ * ds_accept writes them) are copied, in every layer and kv head, K and V,
+ * from slot L + c_i to slot L + i, and new_ctx_lens[b] = L + 1 + n.  Slots
+ * past the new length keep stale data that the length excludes.  A sequence
+ * without a tree gets new_ctx_lens[b] = L.
+ *
+ * Device-side checks (status bits in the workspace, see ds_device_status):
+ * a path that is not strictly increasing inside (0, T) or n outside
+ * [0, T-1] sets DS_DEV_BAD_TREE and commits the root only (L + 1); a page id
+ * outside [0, num_pages) sets DS_DEV_BAD_PAGE and that slot is skipped;
+ * L + T beyond max_pages * page_size sets DS_DEV_BAD_LENGTH and the sequence
+ * keeps L.  Refused on the host: num_layers outside 1..DS_MAX_COMMIT_LAYERS,
+ * head_dim not 64 or 128, page_size not 16/32/64/128, new_ctx_lens == ctx_lens.
+ * Caches as in ds_verify_attn (same layout for all layers), 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+#define DS_MAX_COMMIT_LAYERS 128
+
+typedef struct ds_commit_args {
+  void* const*   k_caches;      /* host array [num_layers] of device pointers   */
+  void* const*   v_caches;      /* host array [num_layers] of device pointers   */
+  int32_t        num_layers;
+  const int32_t* page_table;    /* [batch, max_pages]                           */
+  const int32_t* ctx_lens;      /* [batch]                                      */
+  const int32_t* tree_offsets;  /* [batch + 1]                                  */
+  const int32_t* path;          /* [batch, DS_MAX_TREE_NODES] from ds_accept    */
+  const int32_t* n_accepted;    /* [batch]                                      */
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_pages;
+  int32_t kv_layout;            /* ds_kv_layout                                 */
+  int32_t* new_ctx_lens;        /* [batch] out; must not alias ctx_lens         */
+  void*   workspace;            /* >= 256 bytes: the status word                */
+  size_t  workspace_bytes;
+} ds_commit_args;
+
+void ds_commit_args_default(ds_commit_args* args);
+ds_status ds_kv_commit(const ds_commit_args* args, void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

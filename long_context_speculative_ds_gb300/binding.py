@@ -64,6 +64,16 @@ class AcceptArgs(C.Structure):
                 ("workspace_bytes", C.c_size_t)]
 
 
+class CommitArgs(C.Structure):
+    _fields_ = [("k_caches", C.POINTER(_p)), ("v_caches", C.POINTER(_p)),
+                ("num_layers", _i), ("page_table", _p), ("ctx_lens", _p),
+                ("tree_offsets", _p), ("path", _p), ("n_accepted", _p),
+                ("batch", _i), ("num_kv_heads", _i), ("head_dim", _i),
+                ("page_size", _i), ("num_pages", _i), ("max_pages", _i),
+                ("kv_layout", _i), ("new_ctx_lens", _p), ("workspace", _p),
+                ("workspace_bytes", C.c_size_t)]
+
+
 class DSError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"ds status {status}: {message}")
@@ -78,7 +88,7 @@ EXPORTS = ("ds_last_error", "ds_abi_version", "ds_struct_size",
            "ds_verify_attn", "ds_gather_args_default",
            "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
            "ds_accept_args_default", "ds_accept_workspace_size", "ds_accept",
-           "ds_accept_static")
+           "ds_accept_static", "ds_commit_args_default", "ds_kv_commit")
 
 
 def lib_path() -> str:
@@ -103,9 +113,10 @@ def load(path: Optional[str] = None) -> C.CDLL:
     for name in ("ds_workspace_init", "ds_device_status",
                  "ds_verify_attn_workspace_size", "ds_verify_attn",
                  "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
-                 "ds_accept_workspace_size", "ds_accept", "ds_accept_static"):
+                 "ds_accept_workspace_size", "ds_accept", "ds_accept_static",
+                 "ds_kv_commit"):
         getattr(lib, name).restype = C.c_int
-    for which, cls in enumerate((VerifyArgs, GatherArgs, AcceptArgs)):
+    for which, cls in enumerate((VerifyArgs, GatherArgs, AcceptArgs, CommitArgs)):
         got = lib.ds_struct_size(which)
         if got != C.sizeof(cls):
             raise RuntimeError(f"struct {cls.__name__}: library has {got} bytes,"
@@ -270,6 +281,38 @@ def ds_accept_static(args: AcceptArgs, stream=None, read_flags: bool = True):
                                    C.byref(flags) if read_flags else None,
                                    _stream(stream)))
     return flags.value if read_flags else None
+
+
+def commit_args(k_caches, v_caches, page_table, ctx_lens, tree_offsets, path,
+                n_accepted, *, new_ctx_lens, workspace,
+                kv_layout: str = "NHD") -> CommitArgs:
+    """Arguments of ds_kv_commit.  k_caches / v_caches are lists of the
+    layers' paged caches; the pointer arrays live in the returned struct
+    (kept alive by it) and are read on the host at call time."""
+    a = CommitArgs()
+    load().ds_commit_args_default(C.byref(a))
+    nl = len(k_caches)
+    kp = (_p * nl)(*[t.data_ptr() for t in k_caches])
+    vp = (_p * nl)(*[t.data_ptr() for t in v_caches])
+    a._keep = (kp, vp)
+    a.k_caches = C.cast(kp, C.POINTER(_p))
+    a.v_caches = C.cast(vp, C.POINTER(_p))
+    a.num_layers = nl
+    num_pages, page_size, kv_heads, head_dim = _cache_dims(k_caches[0], kv_layout)
+    a.page_table, a.ctx_lens = _ptr(page_table), _ptr(ctx_lens)
+    a.tree_offsets, a.path, a.n_accepted = _ptr(tree_offsets), _ptr(path), _ptr(n_accepted)
+    a.batch = page_table.shape[0]
+    a.num_kv_heads, a.head_dim, a.page_size = kv_heads, head_dim, page_size
+    a.num_pages, a.max_pages = num_pages, page_table.shape[1]
+    a.kv_layout = _LAYOUT[kv_layout]
+    a.new_ctx_lens = _ptr(new_ctx_lens)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def ds_kv_commit(args: CommitArgs, stream=None):
+    _check(load().ds_kv_commit(C.byref(args), _stream(stream)))
 
 
 def ds_workspace_init(workspace: torch.Tensor, stream=None):

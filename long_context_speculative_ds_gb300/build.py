@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB_NAME = "libds_verify.so"
 SOURCES = ["abi.cpp", "verify_attn.cu", "verify_tc.cu", "topk_gather.cu",
-           "accept.cu", "accept_static.cu"]
+           "accept.cu", "accept_static.cu", "kv_commit.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "-I" + INCLUDE, "-I" + CSRC]

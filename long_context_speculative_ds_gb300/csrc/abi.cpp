@@ -99,19 +99,19 @@ namespace ds {
 VerifyLayout verify_layout(const ds_verify_args& a, int num_sms) {
   VerifyLayout L;
   L.group = a.num_q_heads / a.num_kv_heads;
-  L.rg_max = (DS_MAX_TREE_NODES * L.group + 255) / 256;
+  L.rg_max = (DS_MAX_TREE_NODES * L.group + kRowsPerItem - 1) / kRowsPerItem;
   L.target_ctas = num_sms;
   L.max_items = num_sms + a.batch * a.num_kv_heads * L.rg_max;
   size_t off = kStatusBytes;
   L.o_part = off;
-  off = align_up(off + (size_t)L.max_items * 256 * a.head_dim * sizeof(float));
+  off = align_up(off + (size_t)L.max_items * kRowsPerItem * a.head_dim * sizeof(float));
   L.lse_part = off;
-  off = align_up(off + (size_t)L.max_items * 256 * sizeof(float));
+  off = align_up(off + (size_t)L.max_items * kRowsPerItem * sizeof(float));
   L.clse = off;
-  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * a.max_chunks * 256 *
+  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * a.max_chunks * kRowsPerItem *
                            sizeof(float));
   L.row_lse = off;
-  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * 256 * sizeof(float));
+  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * kRowsPerItem * sizeof(float));
   L.total = off;
   return L;
 }
@@ -141,6 +141,7 @@ int64_t ds_struct_size(int32_t which) {
     case 0: return (int64_t)sizeof(ds_verify_args);
     case 1: return (int64_t)sizeof(ds_gather_args);
     case 2: return (int64_t)sizeof(ds_accept_args);
+    case 3: return (int64_t)sizeof(ds_commit_args);
     default: return -1;
   }
 }
@@ -324,6 +325,48 @@ ds_status ds_accept(const ds_accept_args* a, void* stream) {
           "workspace_bytes %zu < required %zu", a->workspace_bytes, L.total);
   cudaError_t e = ds::launch_accept(*a, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ds_accept launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
+void ds_commit_args_default(ds_commit_args* a) {
+  if (!a) return;
+  std::memset(a, 0, sizeof(*a));
+  a->kv_layout = DS_KV_NHD;
+}
+
+ds_status ds_kv_commit(const ds_commit_args* a, void* stream) {
+  REQUIRE(a, DS_ERR_INVALID_ARG, "args is NULL");
+  REQUIRE(a->num_layers >= 1 && a->num_layers <= DS_MAX_COMMIT_LAYERS, DS_ERR_UNSUPPORTED,
+          "num_layers %d outside 1..%d", a->num_layers, DS_MAX_COMMIT_LAYERS);
+  REQUIRE(a->k_caches && a->v_caches, DS_ERR_INVALID_ARG, "k_caches/v_caches is NULL");
+  for (int l = 0; l < a->num_layers; ++l) {
+    REQUIRE(a->k_caches[l] && a->v_caches[l], DS_ERR_INVALID_ARG,
+            "k_caches[%d]/v_caches[%d] is NULL", l, l);
+    REQUIRE(aligned16(a->k_caches[l]) && aligned16(a->v_caches[l]), DS_ERR_INVALID_ARG,
+            "caches of layer %d must be 16-byte aligned", l);
+  }
+  REQUIRE(a->batch >= 1, DS_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", a->batch);
+  REQUIRE(a->num_kv_heads >= 1, DS_ERR_INVALID_ARG, "num_kv_heads must be >= 1");
+  REQUIRE(a->head_dim == 64 || a->head_dim == 128, DS_ERR_UNSUPPORTED,
+          "head_dim %d (64 or 128)", a->head_dim);
+  REQUIRE(a->page_size == 16 || a->page_size == 32 || a->page_size == 64 ||
+              a->page_size == 128,
+          DS_ERR_UNSUPPORTED, "page_size %d (16, 32, 64 or 128)", a->page_size);
+  REQUIRE(a->num_pages >= 1 && a->max_pages >= 1, DS_ERR_INVALID_ARG,
+          "num_pages and max_pages must be >= 1");
+  REQUIRE(a->kv_layout == DS_KV_NHD || a->kv_layout == DS_KV_HND, DS_ERR_INVALID_ARG,
+          "kv_layout %d is not a ds_kv_layout", a->kv_layout);
+  REQUIRE(a->page_table && a->ctx_lens && a->tree_offsets && a->path && a->n_accepted,
+          DS_ERR_INVALID_ARG, "page_table/ctx_lens/tree_offsets/path/n_accepted is NULL");
+  REQUIRE(a->new_ctx_lens, DS_ERR_INVALID_ARG, "new_ctx_lens is NULL");
+  REQUIRE((const void*)a->new_ctx_lens != (const void*)a->ctx_lens, DS_ERR_INVALID_ARG,
+          "new_ctx_lens must not alias ctx_lens");
+  REQUIRE(a->workspace, DS_ERR_WORKSPACE, "workspace is NULL");
+  REQUIRE(a->workspace_bytes >= ds::kStatusBytes, DS_ERR_WORKSPACE,
+          "workspace_bytes %zu < %zu", a->workspace_bytes, ds::kStatusBytes);
+  cudaError_t e = ds::launch_kv_commit(*a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ds_kv_commit launch");
   return ok();
 }
 

@@ -6,13 +6,14 @@
 #include <stdint.h>
 
 #include "ds.h"
+#include "internal.h"
 
 #define DS_DEV __device__ __forceinline__
 
 namespace ds {
 
 constexpr int kTileKeys = 128;       // keys per attention tile
-constexpr int kRowsPerGroup = 256;   // query rows per work item (2 x 128)
+constexpr int kRowsPerGroup = DS_ROWS_PER_ITEM;   // query rows per work item
 constexpr float kLog2e = 1.4426950408889634f;
 
 DS_DEV void flag(uint32_t* status, uint32_t bits) {

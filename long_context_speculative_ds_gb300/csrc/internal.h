@@ -9,6 +9,12 @@
 
 namespace ds {
 
+#ifndef DS_ROWS_PER_ITEM
+#define DS_ROWS_PER_ITEM 256
+#endif
+// query rows per split-pass work item (128 or 256)
+constexpr int kRowsPerItem = DS_ROWS_PER_ITEM;
+
 constexpr size_t kAlign = 256;
 constexpr size_t kStatusBytes = 256;   // status word region at workspace start
 
@@ -50,6 +56,8 @@ cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
 cudaError_t launch_topk_gather(const ds_gather_args& a, cudaStream_t stream);
 cudaError_t launch_accept(const ds_accept_args& a, const AcceptLayout& L,
                           cudaStream_t stream);
+
+cudaError_t launch_kv_commit(const ds_commit_args& a, cudaStream_t stream);
 
 // Sets the message ds_last_error returns on this thread; returns st.
 ds_status set_last_error(ds_status st, const char* msg);

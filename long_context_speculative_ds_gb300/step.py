@@ -1,6 +1,7 @@
 """One verify step through the C ABI: per-layer tree-verify attention with
 chunk salience summed over layers, then top-k chunk gather into the compact
-draft cache, then tree acceptance.
+draft cache, then tree acceptance, then (optionally) the commit of the
+accepted path into every layer's cache.
 
 `VerifyStep` owns the device buffers of a step (outputs and workspaces) for
 fixed sizes; every computation is a call into the library.  Inputs are passed
@@ -43,7 +44,7 @@ class VerifyStep:
     def __init__(self, inp: StepInputs, *, chunk_size: int, top_k: int,
                  window: int, accept_mode: str, kv_layout: str = "NHD",
                  out_dtype: torch.dtype = torch.bfloat16, num_sms: int = 0,
-                 device: str = "cuda"):
+                 device: str = "cuda", with_commit: bool = False):
         self.inp = inp
         self.chunk_size, self.top_k, self.window = chunk_size, top_k, window
         self.accept_mode = accept_mode
@@ -111,7 +112,16 @@ class VerifyStep:
             out_n_accepted=self.out_n, out_bonus=self.out_bonus,
             draft_logits=inp.draft_logits, uniforms=inp.uniforms,
             workspace=self.ws_accept)
-        for ws in (self.ws_verify, self.ws_gather, self.ws_accept):
+        self.with_commit = with_commit
+        self.new_ctx_lens = torch.empty(bsz, dtype=torch.int32, device=dev)
+        self.ws_commit = torch.zeros(256, dtype=torch.uint8, device=dev)
+        if with_commit:
+            self.commit_args = B.commit_args(
+                inp.k_cache, inp.v_cache, inp.page_table, inp.ctx_lens,
+                inp.tree_offsets, self.out_path, self.out_n,
+                new_ctx_lens=self.new_ctx_lens, workspace=self.ws_commit,
+                kv_layout=kv_layout)
+        for ws in (self.ws_verify, self.ws_gather, self.ws_accept, self.ws_commit):
             B.ds_workspace_init(ws)
 
     # -- the step ----------------------------------------------------------
@@ -124,21 +134,27 @@ class VerifyStep:
     def accept(self, stream=None):
         B.ds_accept(self.accept_args, stream)
 
+    def commit(self, stream=None):
+        B.ds_kv_commit(self.commit_args, stream)
+
     def run(self, stream=None):
         for l in range(self.layers):
             self.verify_layer(l, stream)
         self.gather(stream)
         self.accept(stream)
+        if self.with_commit:
+            self.commit(stream)
 
     def launches_per_step(self) -> int:
         """Kernel launches of one step: 3 per layer (split pass, combine,
-        chunk finalize), 2 for top-k + gather, 2 for acceptance."""
+        chunk finalize), 2 for top-k + gather, 2 for acceptance, 1 for the
+        commit."""
         fin = 1 if self.max_chunks > 0 else 0
-        return self.layers * (2 + fin) + 2 + 2
+        return self.layers * (2 + fin) + 2 + 2 + (1 if self.with_commit else 0)
 
     def device_status(self) -> int:
         s = 0
-        for ws in (self.ws_verify, self.ws_gather, self.ws_accept):
+        for ws in (self.ws_verify, self.ws_gather, self.ws_accept, self.ws_commit):
             s |= B.ds_device_status(ws)
         return s
 
