@@ -26,6 +26,9 @@ step, with no blocking, fusion or reordering:
     Does", last paragraph: "combined with a rolling recent window, and rebuilt
     as a compact ... cache"; CGCL-codes/DiffSpec README, "Features": chunk
     arena, "physically contiguous chunk staging").
+  * rope_rotate / f64_to_bf16_bits: with a RoPE base the gathered pre-RoPE
+    K is rotated to its local position in the compact cache (half-split
+    pairing, inverse frequencies base^(-2j/D)) and rounded once to bf16.
   * greedy_accept: accept-if-equal against the target argmax, walking the tree
     from the root (vllm.cpp docs "Speculative decoding", section "MTP":
     "greedy decoding plus accept-if-equal rejection").
@@ -191,12 +194,42 @@ def working_set_positions(chunks: Sequence[int], L: int, chunk_size: int,
     return pos
 
 
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even), in one step
+    (no intermediate float32 rounding); returns uint16 bit patterns.  Finite
+    normal-range inputs only."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                 # x = m * 2^e, 0.5 <= |m| < 1
+    q = np.rint(m * 256.0)             # 8 significant bits, ties to even
+    r = np.ldexp(q / 256.0, e)         # exactly representable in bf16
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def rope_rotate(x, pos: int, base: float) -> np.ndarray:
+    """Rotary position embedding of the rows x[..., D] at position `pos`, in
+    float64: pair (j, j + D/2) is rotated by the angle pos * base^(-2j/D),
+    j < D/2 (the half-split pairing).  Returns float64 (no rounding)."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    j = np.arange(D // 2, dtype=np.float64)
+    ang = pos * base ** (-2.0 * j / D)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., :D // 2], x[..., D // 2:]
+    return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+
+
 def gather_compact(src_k_bits, src_v_bits, page_table, ctx_lens, scores,
                    page_size: int, chunk_size: int, top_k: int, window: int,
-                   capacity: int, layout: str = "NHD"):
+                   capacity: int, layout: str = "NHD", rope_base: float = 0.0):
     """Returns dict with chunk_ids [B, top_k] (-1 padded), positions [B, cap]
     (-1 padded), out_len [B], out_k/out_v [B, cap, H_kv, D] uint16 bits (zero
-    beyond out_len)."""
+    beyond out_len).
+
+    With rope_base > 0 the source K is taken to be pre-RoPE and compact row i
+    gets RoPE at its local position i (rounded once to bf16): the compact
+    cache is rebuilt with local draft positions (vllm-diffspec README,
+    "Architecture", dual-view draft cache; "What DiffSpec Does", last
+    paragraph).  V is copied unchanged."""
     src_k_bits = np.asarray(src_k_bits)
     src_v_bits = np.asarray(src_v_bits)
     B = len(ctx_lens)
@@ -225,6 +258,9 @@ def gather_compact(src_k_bits, src_v_bits, page_table, ctx_lens, scores,
             else:
                 out_k[b, i] = src_k_bits[page, :, off]
                 out_v[b, i] = src_v_bits[page, :, off]
+            if rope_base > 0:
+                out_k[b, i] = f64_to_bf16_bits(
+                    rope_rotate(bf16_bits_to_f64(out_k[b, i]), i, rope_base))
     return dict(chunk_ids=chunk_ids, positions=positions, out_len=out_len,
                 out_k=out_k, out_v=out_v)
 
