@@ -216,6 +216,7 @@ def _config(wl, st, kv_layout="NHD"):
             "head_dim": wl.head_dim, "page_size": wl.page_size,
             "chunk_size": wl.chunk_size, "top_k": wl.top_k,
             "window": wl.window, "vocab": wl.vocab, "accept": wl.accept,
+            "rope_base": wl.rope_base, "kv_commit": True,
             "l2": "inputs larger than L2: every layer has its own "
                   f"{_kv_bytes(wl, st) / 1e6:.0f} MB K/V cache"}
 
@@ -304,7 +305,8 @@ def run_ours(args, wl, rank, world, local_rank):
                      draft_tokens=acc.draft_tokens, uniforms=acc.uniforms)
     step = VerifyStep(inp, chunk_size=wl.chunk_size, top_k=wl.top_k,
                       window=wl.window, accept_mode=mode,
-                      kv_layout=args.kv_layout, with_commit=True)
+                      kv_layout=args.kv_layout, with_commit=True,
+                      rope_base=wl.rope_base)
     # per-layer events around the split-pass kernel
     n_ev = args.steps * wl.layers
     evs = [(torch.cuda.Event(enable_timing=True),

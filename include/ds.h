@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define DS_ABI_VERSION 1
+#define DS_ABI_VERSION 2
 /* Largest draft tree per sequence: one 64-bit ancestor mask per node. */
 #define DS_MAX_TREE_NODES 64
 
@@ -195,6 +195,16 @@ ds_status ds_verify_attn(const ds_verify_args* args, void* stream);
  *   out_positions[b, i] = -1 for i >= out_len[b]; out_k/out_v rows beyond
  *   out_len[b] are left untouched.
  *
+ *   With rope_base > 0 the source K is pre-RoPE and the compact cache is
+ *   rebuilt with local positions (vllm-diffspec README, "Architecture":
+ *   dual-view draft cache, canonical pre-RoPE KV at absolute positions and a
+ *   compact cache with local draft RoPE positions): row i of out_k is the
+ *   source row rotated to position i, pair (j, j + D/2) by the angle
+ *   i * rope_base^(-2j/D), j < D/2, rounded to bf16.  The angle is formed
+ *   and reduced modulo 2 pi in float64 and rotated in float32, so a value
+ *   can differ from the exactly rounded result by one bf16 unit.  V is
+ *   always copied byte for byte; rope_base = 0 copies K byte for byte too.
+ *
  * Constraints: chunk_size a multiple of page_size; head_dim 64 or 128;
  * capacity >= top_k * chunk_size + window.
  * ------------------------------------------------------------------------ */
@@ -223,6 +233,7 @@ typedef struct ds_gather_args {
   int32_t* out_chunk_ids;       /* [batch, top_k]                              */
   void*   workspace;            /* scratch, >= ds_chunk_topk_gather_workspace_size */
   size_t  workspace_bytes;
+  float   rope_base;            /* 0: no rotation; > 0: RoPE base (theta)      */
 } ds_gather_args;
 
 void ds_gather_args_default(ds_gather_args* args);

@@ -52,7 +52,8 @@ class GatherArgs(C.Structure):
                 ("window", _i), ("capacity", _i),
                 ("out_k", _p), ("out_v", _p), ("out_positions", _p),
                 ("out_len", _p), ("out_chunk_ids", _p),
-                ("workspace", _p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", _p), ("workspace_bytes", C.c_size_t),
+                ("rope_base", C.c_float)]
 
 
 class AcceptArgs(C.Structure):
@@ -210,7 +211,7 @@ def ds_verify_attn(args: VerifyArgs, stream=None):
 def gather_args(scores, ctx_lens, src_k, src_v, page_table, *, chunk_size: int,
                 top_k: int, window: int, out_k, out_v, out_positions, out_len,
                 out_chunk_ids, workspace=None, kv_layout: str = "NHD",
-                ) -> GatherArgs:
+                rope_base: float = 0.0) -> GatherArgs:
     a = GatherArgs()
     load().ds_gather_args_default(C.byref(a))
     num_pages, page_size, kv_heads, head_dim = _cache_dims(src_k, kv_layout)
@@ -226,6 +227,7 @@ def gather_args(scores, ctx_lens, src_k, src_v, page_table, *, chunk_size: int,
     a.out_k, a.out_v = _ptr(out_k), _ptr(out_v)
     a.out_positions, a.out_len = _ptr(out_positions), _ptr(out_len)
     a.out_chunk_ids = _ptr(out_chunk_ids)
+    a.rope_base = rope_base
     if workspace is not None:
         a.workspace = _ptr(workspace)
         a.workspace_bytes = workspace.numel() * workspace.element_size()

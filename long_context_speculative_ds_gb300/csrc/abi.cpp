@@ -241,6 +241,8 @@ static ds_status check_gather(const ds_gather_args* a) {
           "num_pages and max_pages must be >= 1");
   REQUIRE(a->kv_layout == DS_KV_NHD || a->kv_layout == DS_KV_HND, DS_ERR_INVALID_ARG,
           "kv_layout %d is not a ds_kv_layout", a->kv_layout);
+  REQUIRE(a->rope_base >= 0.f && a->rope_base < 3.0e38f, DS_ERR_INVALID_ARG,
+          "rope_base must be 0 (no rotation) or a finite positive base");
   REQUIRE((int64_t)a->capacity >= (int64_t)a->top_k * a->chunk_size + a->window,
           DS_ERR_INVALID_ARG, "capacity %d < top_k*chunk_size + window = %lld",
           a->capacity, (long long)a->top_k * a->chunk_size + a->window);

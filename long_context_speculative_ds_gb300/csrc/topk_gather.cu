@@ -11,6 +11,8 @@
 //   ids in ascending order, which is also the order of the working set.
 // gather: one warp per compact row; 16-byte vector copies of the token's
 //   K and V (all kv heads) from the paged source into [B, cap, H, D].
+#include <cmath>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +36,8 @@ struct GatherKArgs {
   int32_t* out_len;
   int32_t* out_chunk_ids;
   uint32_t* status;
+  float rope_base;           // > 0: rotate K to its local position
+  double inv_freq[64];       // rope_base^(-2j/D), j < D/2 (host-computed)
 };
 
 constexpr int kSelThreads = 1024;
@@ -201,17 +205,83 @@ __global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
   const int vec_per_head = a.head_dim / 8;            // 16-byte vectors
   const int nvec = a.num_kv_heads * vec_per_head;
   const int64_t drow = ((int64_t)b * a.capacity + i) * a.num_kv_heads * a.head_dim;
+  const int64_t srow = (int64_t)pg * a.page_stride + (int64_t)off * a.tok_stride;
+  const bool rope = a.rope_base > 0.f;
   for (int e = lane; e < nvec; e += 32) {
     const int h = e / vec_per_head, vv = e % vec_per_head;
     uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
     if (pg >= 0) {
-      const int64_t so = (int64_t)pg * a.page_stride + (int64_t)off * a.tok_stride +
-                         (int64_t)h * a.head_stride + vv * 8;
-      kx = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
+      const int64_t so = srow + (int64_t)h * a.head_stride + vv * 8;
+      if (!rope) kx = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
       vx = __ldg(reinterpret_cast<const uint4*>(a.src_v + so));
     }
-    reinterpret_cast<uint4*>(a.out_k + drow)[e] = kx;
+    if (!rope) reinterpret_cast<uint4*>(a.out_k + drow)[e] = kx;
     reinterpret_cast<uint4*>(a.out_v + drow)[e] = vx;
+  }
+  if (!rope) return;
+
+  // K rotated to local position i.  The angle i * base^(-2j/D) is formed and
+  // reduced modulo 2 pi in float64 (positions reach tens of thousands of
+  // radians), then its sine and cosine are taken in float32 and the pair
+  // (j, j + D/2) rotated in float32 and rounded to bf16.  Lane l holds the
+  // sine and cosine of pairs l and l + 32.
+  const int half = a.head_dim / 2;
+  float cq[2], sq[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int j = lane + 32 * q;
+    cq[q] = 1.f;
+    sq[q] = 0.f;
+    if (j < half) {
+      const double ang = (double)i * a.inv_freq[j];
+      const double k = rint(ang * 0.15915494309189535);           // 1 / (2 pi)
+      const float r = (float)fma(-k, 6.283185307179586, ang);      // in [-pi, pi]
+      sincosf(r, &sq[q], &cq[q]);
+    }
+  }
+  // units of (kv head, block of 8 pairs), the whole warp in step so that
+  // every lane takes part in every shuffle
+  const int nb = half / 8;
+  const int units = a.num_kv_heads * nb;
+  for (int u0 = 0; u0 < units; u0 += 32) {
+    const int u = u0 + lane;
+    const bool valid = u < units;
+    const int h = valid ? u / nb : 0, j0 = valid ? (u % nb) * 8 : 0;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (valid && pg >= 0) {
+      const int64_t so = srow + (int64_t)h * a.head_stride + j0;
+      lo = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
+      hi = __ldg(reinterpret_cast<const uint4*>(a.src_k + so + half));
+    }
+    const uint32_t* lw = reinterpret_cast<const uint32_t*>(&lo);
+    const uint32_t* hw = reinterpret_cast<const uint32_t*>(&hi);
+    uint32_t ow_lo[4], ow_hi[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      float xo[2], yo[2];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int j = j0 + 2 * e2 + p;
+        const float c0 = __shfl_sync(0xffffffffu, cq[0], j & 31);
+        const float c1 = __shfl_sync(0xffffffffu, cq[1], j & 31);
+        const float s0 = __shfl_sync(0xffffffffu, sq[0], j & 31);
+        const float s1 = __shfl_sync(0xffffffffu, sq[1], j & 31);
+        const float c = j < 32 ? c0 : c1, sn = j < 32 ? s0 : s1;
+        const float x = __uint_as_float((p ? (lw[e2] >> 16) : (lw[e2] & 0xffffu)) << 16);
+        const float y = __uint_as_float((p ? (hw[e2] >> 16) : (hw[e2] & 0xffffu)) << 16);
+        xo[p] = fmaf(x, c, -y * sn);
+        yo[p] = fmaf(x, sn, y * c);
+      }
+      ow_lo[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xo[0])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xo[1])) << 16);
+      ow_hi[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yo[0])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yo[1])) << 16);
+    }
+    if (valid) {
+      uint16_t* dk = a.out_k + drow + (int64_t)h * a.head_dim + j0;
+      *reinterpret_cast<uint4*>(dk) = make_uint4(ow_lo[0], ow_lo[1], ow_lo[2], ow_lo[3]);
+      *reinterpret_cast<uint4*>(dk + half) = make_uint4(ow_hi[0], ow_hi[1], ow_hi[2], ow_hi[3]);
+    }
   }
 }
 
@@ -238,6 +308,11 @@ cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
   a.out_len = g.out_len;
   a.out_chunk_ids = g.out_chunk_ids;
   a.status = static_cast<uint32_t*>(g.workspace);
+  a.rope_base = g.rope_base;
+  for (int j = 0; j < 64; ++j)
+    a.inv_freq[j] = (g.rope_base > 0.f && j < g.head_dim / 2)
+                        ? std::pow((double)g.rope_base, -2.0 * j / g.head_dim)
+                        : 0.0;
   topk_select<<<g.batch, kSelThreads, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -44,7 +44,8 @@ class VerifyStep:
     def __init__(self, inp: StepInputs, *, chunk_size: int, top_k: int,
                  window: int, accept_mode: str, kv_layout: str = "NHD",
                  out_dtype: torch.dtype = torch.bfloat16, num_sms: int = 0,
-                 device: str = "cuda", with_commit: bool = False):
+                 device: str = "cuda", with_commit: bool = False,
+                 rope_base: float = 0.0):
         self.inp = inp
         self.chunk_size, self.top_k, self.window = chunk_size, top_k, window
         self.accept_mode = accept_mode
@@ -93,7 +94,7 @@ class VerifyStep:
             out_k=self.out_k, out_v=self.out_v,
             out_positions=self.out_positions, out_len=self.out_len,
             out_chunk_ids=self.out_chunk_ids, workspace=self.ws_gather,
-            kv_layout=kv_layout)
+            kv_layout=kv_layout, rope_base=rope_base)
         self.out_path = torch.empty(bsz, B.DS_MAX_TREE_NODES, dtype=torch.int32,
                                     device=dev)
         self.out_n = torch.empty(bsz, dtype=torch.int32, device=dev)

@@ -63,6 +63,9 @@ class Workload:
     draft: Optional[str]                   # None, "iid" or "noisy"
     ctx_range: Sequence[int] = (4096, 131072)
     tree_range: Sequence[int] = (16, 64)
+    # RoPE base of the draft's compact cache (the model family's rotary theta:
+    # 500000 for Llama 3.1, 1000000 for Qwen3, 10000 for the tiny case)
+    rope_base: float = 10000.0
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -73,16 +76,17 @@ WORKLOADS = {
                      32, 4, 64, 256, "both", 0, "iid"),
     "llama8b-32k": Workload("llama8b-32k", 2, 1, 32, 8, 128, 1, 16, (32768,),
                             (32,), 8, 3, 64, 64, 1024, 128256, "greedy", 16,
-                            None),
+                            None, rope_base=500000.0),
     "llama8b-64k": Workload("llama8b-64k", 3, 1, 32, 8, 128, 1, 16, (65536,),
                             (64,), 10, 4, 64, 128, 2048, 128256, "reject", 32,
-                            "noisy"),
+                            "noisy", rope_base=500000.0),
     "llama8b-128k-32l": Workload("llama8b-128k-32l", 4, 1, 32, 8, 128, 32, 16,
                                  (131072,), (64,), 10, 4, 64, 256, 2048,
-                                 128256, "greedy", 32, None),
+                                 128256, "greedy", 32, None, rope_base=500000.0),
     "qwen3-8b-ragged-b8": Workload("qwen3-8b-ragged-b8", 5, 8, 32, 8, 128, 36,
                                    16, None, None, 10, 4, 64, 128, 1024,
-                                   151936, "reject", 0, "noisy"),
+                                   151936, "reject", 0, "noisy",
+                                   rope_base=1000000.0),
 }
 
 

@@ -38,10 +38,11 @@ def test_exports_every_declared_function(lib):
 
 
 def test_struct_layouts_and_version(lib):
-    assert lib.ds_abi_version() == 1
+    assert lib.ds_abi_version() == 2
     assert lib.ds_struct_size(0) == C.sizeof(B.VerifyArgs)
     assert lib.ds_struct_size(1) == C.sizeof(B.GatherArgs)
     assert lib.ds_struct_size(2) == C.sizeof(B.AcceptArgs)
+    assert lib.ds_struct_size(3) == C.sizeof(B.CommitArgs)
     assert lib.ds_struct_size(7) == -1
 
 
@@ -108,6 +109,11 @@ def test_gather_and_accept_refusals(lib):
     assert "capacity" in lib.ds_last_error().decode()
     g.capacity = 4 * 64 + 64
     assert lib.ds_chunk_topk_gather_workspace_size(C.byref(g), C.byref(n)) == B.DS_OK
+    g.rope_base = -1.0
+    assert lib.ds_chunk_topk_gather_workspace_size(C.byref(g), C.byref(n)) == \
+        B.DS_ERR_INVALID_ARG
+    assert "rope_base" in lib.ds_last_error().decode()
+    g.rope_base = 0.0
     g.chunk_size = 40
     assert lib.ds_chunk_topk_gather(C.byref(g), None) == B.DS_ERR_UNSUPPORTED
 

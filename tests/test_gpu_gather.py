@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+from long_context_speculative_ds_gb300 import binding as B
 from long_context_speculative_ds_gb300 import synth
 from oracle import ref
 import helpers as H
@@ -112,3 +113,55 @@ def test_full_size_from_verify_scores(name):
             sk, sk1 = srt[wl.top_k - 1], srt[wl.top_k]
             assert abs(sk - sk1) <= 1e-3 * sk, "selection differs beyond a near-tie"
         assert set(st.planted_chunks[b]) <= set(got), "a planted chunk was missed"
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_gather_with_local_rope(layout, head_dim):
+    """rope_base > 0: K rotated to its local position in the compact cache
+    (vllm-diffspec README, "Architecture", dual-view draft cache).  Selection,
+    positions, lengths and V stay byte-exact.  K against the oracle's
+    once-rounded float64 rotation: the kernel reduces the angle in float64
+    and rotates in float32, an absolute error of at most ~1e-6 of the pair's
+    norm before rounding, so |gpu - ref| <= ulp_bf16(ref) + 1e-6 * |pair|;
+    and nearly every value is equal."""
+    wl = synth.tiny_workload(batch=3, chunk_size=32, top_k=6, window=200,
+                             head_dim=head_dim, num_q_heads=8, num_kv_heads=4)
+    st, inp, mode = H.build_case(wl, layout=layout, seed=9,
+                                 ctx_lens=(3000, 900, 100), tree_sizes=(3, 2, 2))
+    step = H.make_step(wl, inp, mode, layout)
+    rng = np.random.default_rng(3)
+    scores = rng.random(step.scores.shape).astype(np.float32)
+    _set_scores(step, scores)
+    base = 500000.0
+    ga = B.gather_args(step.scores, inp.ctx_lens, inp.src_k, inp.src_v, inp.page_table,
+                       chunk_size=wl.chunk_size, top_k=wl.top_k, window=wl.window,
+                       out_k=step.out_k, out_v=step.out_v,
+                       out_positions=step.out_positions, out_len=step.out_len,
+                       out_chunk_ids=step.out_chunk_ids, workspace=step.ws_gather,
+                       kv_layout=layout, rope_base=base)
+    B.ds_chunk_topk_gather(ga)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    exp = ref.gather_compact(H.bits(inp.src_k), H.bits(inp.src_v), st.page_table.numpy(),
+                             st.ctx_lens, scores.astype(np.float64), wl.page_size,
+                             wl.chunk_size, wl.top_k, wl.window, step.capacity,
+                             layout=layout, rope_base=base)
+    np.testing.assert_array_equal(step.out_len.cpu().numpy(), exp["out_len"])
+    np.testing.assert_array_equal(step.out_positions.cpu().numpy(), exp["positions"])
+    ok, ov = H.bits(step.out_k), H.bits(step.out_v)
+    exact = total = 0
+    for b in range(wl.batch):
+        n = exp["out_len"][b]
+        np.testing.assert_array_equal(ov[b, :n], exp["out_v"][b, :n])
+        g = ref.bf16_bits_to_f64(ok[b, :n])
+        o = ref.bf16_bits_to_f64(exp["out_k"][b, :n])
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o), 1e-30))) - 7)
+        half = head_dim // 2
+        pair = np.sqrt(o[..., :half] ** 2 + o[..., half:] ** 2)
+        pair = np.concatenate([pair, pair], axis=-1)
+        tol = ulp + 1e-6 * pair
+        assert (np.abs(g - o) <= tol).all(), f"seq {b}: max err {np.abs(g - o).max()}"
+        exact += int((ok[b, :n] == exp["out_k"][b, :n]).sum())
+        total += ok[b, :n].size
+    assert exact >= 0.995 * total, (exact, total)
