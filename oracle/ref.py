@@ -32,6 +32,9 @@ step, with no blocking, fusion or reordering:
   * greedy_accept: accept-if-equal against the target argmax, walking the tree
     from the root (vllm.cpp docs "Speculative decoding", section "MTP":
     "greedy decoding plus accept-if-equal rejection").
+  * compact_append: between retrievals the tokens committed since are
+    appended behind the compact cache's last row (vllm-diffspec README,
+    "What DiffSpec Does" item 4; "Configuration", retrieval interval).
   * kv_commit: after acceptance the accepted path's tree K/V move into the
     consecutive slots after the root and the length grows by 1 + n; the
     stale tail is excluded by the length (adaptive-specdec README, "Layout").
@@ -263,6 +266,40 @@ def gather_compact(src_k_bits, src_v_bits, page_table, ctx_lens, scores,
                     rope_rotate(bf16_bits_to_f64(out_k[b, i]), i, rope_base))
     return dict(chunk_ids=chunk_ids, positions=positions, out_len=out_len,
                 out_k=out_k, out_v=out_v)
+
+
+def compact_append(compact: Dict, src_k_bits, src_v_bits, page_table, from_lens,
+                   to_lens, page_size: int, layout: str = "NHD",
+                   rope_base: float = 0.0) -> Dict:
+    """Between retrievals the compact cache is kept and the tokens committed
+    since, [from_lens[b], to_lens[b]), are appended behind its last row, K
+    rotated to the appended rows' local positions (vllm-diffspec README,
+    "What DiffSpec Does" item 4, KV reuse across decoding steps; the
+    retrieval interval of "Configuration").  Returns a new dict; a sequence
+    whose rows would not fit is left unchanged (the caller retrieves anew)."""
+    out = {k: np.array(v, copy=True) for k, v in compact.items()}
+    cap = out["positions"].shape[1]
+    for b in range(len(from_lens)):
+        f, t = int(from_lens[b]), int(to_lens[b])
+        n0 = int(out["out_len"][b])
+        if f < 0 or t < f or n0 + (t - f) > cap:
+            continue
+        for k, pos in enumerate(range(f, t)):
+            i = n0 + k
+            page = int(page_table[b][pos // page_size])
+            off = pos % page_size
+            if layout == "NHD":
+                rk, rv = src_k_bits[page, off], src_v_bits[page, off]
+            else:
+                rk, rv = src_k_bits[page, :, off], src_v_bits[page, :, off]
+            out["out_k"][b, i] = rk
+            out["out_v"][b, i] = rv
+            if rope_base > 0:
+                out["out_k"][b, i] = f64_to_bf16_bits(
+                    rope_rotate(bf16_bits_to_f64(rk), i, rope_base))
+            out["positions"][b, i] = pos
+        out["out_len"][b] = n0 + (t - f)
+    return out
 
 
 # --------------------------------------------------------------------------
