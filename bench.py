@@ -393,6 +393,38 @@ def run_ours(args, wl, rank, world, local_rank):
     commit_us = c0.elapsed_time(c1) * 1e3 / reps
     commit_bytes = sum(n_acc) * wl.num_kv_heads * wl.head_dim * 2 * 2 * 2 * wl.layers
 
+    # compact append between retrievals: the root and the accepted path
+    # (1 + n tokens) appended behind a compact cache with room for them
+    cap2 = step.capacity + 64
+    kvh, hd = wl.num_kv_heads, wl.head_dim
+    a_k = torch.zeros(wl.batch, cap2, kvh, hd, dtype=torch.bfloat16, device=dev)
+    a_v = torch.zeros_like(a_k)
+    a_pos = torch.empty(wl.batch, cap2, **i32)
+    a_len = torch.empty(wl.batch, **i32)
+    a_ids = torch.empty(wl.batch, max(wl.top_k, 1), **i32)
+    a_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    binding.ds_chunk_topk_gather(binding.gather_args(
+        step.scores, inp.ctx_lens, inp.src_k, inp.src_v, inp.page_table,
+        chunk_size=wl.chunk_size, top_k=wl.top_k, window=wl.window, out_k=a_k,
+        out_v=a_v, out_positions=a_pos, out_len=a_len, out_chunk_ids=a_ids,
+        workspace=a_ws, kv_layout=args.kv_layout, rope_base=wl.rope_base))
+    n_app = [1 + n for n in n_acc]
+    to_t = inp.ctx_lens + torch.tensor(n_app, **i32)
+    app_args = binding.append_args(inp.src_k, inp.src_v, inp.page_table, inp.ctx_lens,
+                                   to_t, out_k=a_k, out_v=a_v, out_positions=a_pos,
+                                   out_len=a_len, workspace=a_ws,
+                                   kv_layout=args.kv_layout, rope_base=wl.rope_base)
+    a_reps = max(1, min(5, 64 // max(n_app)))
+    c0.record()
+    for _ in range(a_reps):
+        binding.ds_compact_append(app_args)
+    c1.record()
+    torch.cuda.synchronize()
+    assert binding.ds_device_status(a_ws) == 0
+    append_us = c0.elapsed_time(c1) * 1e3 / a_reps
+    append_bytes = sum(n_app) * kvh * hd * 2 * 2 * 2   # K and V, read + write
+    del a_k, a_v
+
     # end to end: pinned host inputs in, results out, every step
     e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else \
         _end_to_end(step, inp, args, world, dev, barrier)
@@ -434,6 +466,9 @@ def run_ours(args, wl, rank, world, local_rank):
                       "algorithmic_bytes": commit_bytes,
                       "gbs": round(commit_bytes / (commit_us * 1e-6) / 1e9, 1)
                       if commit_us > 0 else None},
+        "compact_append": {"us": round(append_us, 2), "rows": n_app,
+                           "algorithmic_bytes": append_bytes,
+                           "note": "not in the step: the step retrieves every cycle"},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
     }

@@ -13,7 +13,9 @@
  *   ds_accept             the accepted path: greedy accept-if-equal or exact
  *                         tree rejection sampling with supplied uniforms;
  *   ds_kv_commit          the accepted path's tree K/V moved behind the root
- *                         in every layer, and the new context lengths.
+ *                         in every layer, and the new context lengths;
+ *   ds_compact_append     newly committed tokens appended to the compact
+ *                         cache between retrievals.
  *
  * Conventions (all entry points):
  *   - Every pointer named in an args struct is a DEVICE pointer unless its
@@ -82,7 +84,7 @@ const char* ds_last_error(void);
 int32_t ds_abi_version(void);
 
 /* sizeof() of each args struct as compiled into the library: 0 verify,
- * 1 gather, 2 accept, 3 commit; -1 for anything else.  Bindings compare these with
+ * 1 gather, 2 accept, 3 commit, 4 append; -1 for anything else.  Bindings compare these with
  * their own struct layouts before the first call. */
 int64_t ds_struct_size(int32_t which);
 
@@ -318,6 +320,49 @@ ds_status ds_accept(const ds_accept_args* args, void* stream);
 #define DS_ACCEPT_STATIC_MAX_NODES 4096
 ds_status ds_accept_static(const ds_accept_args* args, uint32_t* flags_out,
                            void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * Compact-cache append between retrievals (vllm-diffspec README, "What
+ * DiffSpec Does" item 4: KV reuse and locality across decoding steps, and
+ * "Configuration": diffspec_retrieval_interval, verifier cycles between
+ * retrievals).
+ *
+ * The compact cache built by ds_chunk_topk_gather is kept; for every
+ * sequence b the tokens committed since, t in [from_lens[b], to_lens[b]),
+ * are copied from the paged source cache behind its last row: row
+ * out_len[b] + (t - from_lens[b]) gets token t, out_positions of that row is
+ * t, K is rotated to that row's local position when rope_base > 0 (as in
+ * ds_chunk_topk_gather), and out_len[b] grows by to - from.  If the rows do
+ * not fit in capacity, or from > to, or to is beyond max_pages * page_size,
+ * nothing is appended for b and DS_DEV_BAD_LENGTH is set; a page id outside
+ * [0, num_pages) sets DS_DEV_BAD_PAGE and that row is written as zeros.
+ * Refused on the host: head_dim not 64 or 128, capacity < 0, rope_base < 0.
+ * ------------------------------------------------------------------------ */
+typedef struct ds_append_args {
+  const void*    src_k;         /* paged bf16 source cache (pre-RoPE K)       */
+  const void*    src_v;
+  const int32_t* page_table;    /* [batch, max_pages]                         */
+  const int32_t* from_lens;     /* [batch]                                    */
+  const int32_t* to_lens;       /* [batch]                                    */
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_pages;
+  int32_t kv_layout;
+  int32_t capacity;             /* rows per sequence of the compact cache     */
+  void*    out_k;               /* [batch, capacity, num_kv_heads, head_dim]  */
+  void*    out_v;
+  int32_t* out_positions;       /* [batch, capacity]                          */
+  int32_t* out_len;             /* [batch] rows present; updated in place     */
+  float    rope_base;           /* 0: K copied byte for byte                  */
+  void*   workspace;            /* >= 256 bytes: the status word              */
+  size_t  workspace_bytes;
+} ds_append_args;
+
+void ds_append_args_default(ds_append_args* args);
+ds_status ds_compact_append(const ds_append_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ *
  * Post-accept KV commit (adaptive-specdec README, "Layout": one cache buffer

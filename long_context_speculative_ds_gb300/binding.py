@@ -75,6 +75,16 @@ class CommitArgs(C.Structure):
                 ("workspace_bytes", C.c_size_t)]
 
 
+class AppendArgs(C.Structure):
+    _fields_ = [("src_k", _p), ("src_v", _p), ("page_table", _p),
+                ("from_lens", _p), ("to_lens", _p), ("batch", _i),
+                ("num_kv_heads", _i), ("head_dim", _i), ("page_size", _i),
+                ("num_pages", _i), ("max_pages", _i), ("kv_layout", _i),
+                ("capacity", _i), ("out_k", _p), ("out_v", _p),
+                ("out_positions", _p), ("out_len", _p), ("rope_base", C.c_float),
+                ("workspace", _p), ("workspace_bytes", C.c_size_t)]
+
+
 class DSError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"ds status {status}: {message}")
@@ -89,7 +99,8 @@ EXPORTS = ("ds_last_error", "ds_abi_version", "ds_struct_size",
            "ds_verify_attn", "ds_gather_args_default",
            "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
            "ds_accept_args_default", "ds_accept_workspace_size", "ds_accept",
-           "ds_accept_static", "ds_commit_args_default", "ds_kv_commit")
+           "ds_accept_static", "ds_commit_args_default", "ds_kv_commit",
+           "ds_append_args_default", "ds_compact_append")
 
 
 def lib_path() -> str:
@@ -115,9 +126,10 @@ def load(path: Optional[str] = None) -> C.CDLL:
                  "ds_verify_attn_workspace_size", "ds_verify_attn",
                  "ds_chunk_topk_gather_workspace_size", "ds_chunk_topk_gather",
                  "ds_accept_workspace_size", "ds_accept", "ds_accept_static",
-                 "ds_kv_commit"):
+                 "ds_kv_commit", "ds_compact_append"):
         getattr(lib, name).restype = C.c_int
-    for which, cls in enumerate((VerifyArgs, GatherArgs, AcceptArgs, CommitArgs)):
+    for which, cls in enumerate((VerifyArgs, GatherArgs, AcceptArgs, CommitArgs,
+                                 AppendArgs)):
         got = lib.ds_struct_size(which)
         if got != C.sizeof(cls):
             raise RuntimeError(f"struct {cls.__name__}: library has {got} bytes,"
@@ -315,6 +327,31 @@ def commit_args(k_caches, v_caches, page_table, ctx_lens, tree_offsets, path,
 
 def ds_kv_commit(args: CommitArgs, stream=None):
     _check(load().ds_kv_commit(C.byref(args), _stream(stream)))
+
+
+def append_args(src_k, src_v, page_table, from_lens, to_lens, *, out_k, out_v,
+                out_positions, out_len, workspace, kv_layout: str = "NHD",
+                rope_base: float = 0.0) -> AppendArgs:
+    a = AppendArgs()
+    load().ds_append_args_default(C.byref(a))
+    num_pages, page_size, kv_heads, head_dim = _cache_dims(src_k, kv_layout)
+    a.src_k, a.src_v, a.page_table = _ptr(src_k), _ptr(src_v), _ptr(page_table)
+    a.from_lens, a.to_lens = _ptr(from_lens), _ptr(to_lens)
+    a.batch = page_table.shape[0]
+    a.num_kv_heads, a.head_dim, a.page_size = kv_heads, head_dim, page_size
+    a.num_pages, a.max_pages = num_pages, page_table.shape[1]
+    a.kv_layout = _LAYOUT[kv_layout]
+    a.capacity = out_k.shape[1]
+    a.out_k, a.out_v = _ptr(out_k), _ptr(out_v)
+    a.out_positions, a.out_len = _ptr(out_positions), _ptr(out_len)
+    a.rope_base = rope_base
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def ds_compact_append(args: AppendArgs, stream=None):
+    _check(load().ds_compact_append(C.byref(args), _stream(stream)))
 
 
 def ds_workspace_init(workspace: torch.Tensor, stream=None):

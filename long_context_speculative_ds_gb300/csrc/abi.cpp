@@ -142,6 +142,7 @@ int64_t ds_struct_size(int32_t which) {
     case 1: return (int64_t)sizeof(ds_gather_args);
     case 2: return (int64_t)sizeof(ds_accept_args);
     case 3: return (int64_t)sizeof(ds_commit_args);
+    case 4: return (int64_t)sizeof(ds_append_args);
     default: return -1;
   }
 }
@@ -369,6 +370,42 @@ ds_status ds_kv_commit(const ds_commit_args* a, void* stream) {
           "workspace_bytes %zu < %zu", a->workspace_bytes, ds::kStatusBytes);
   cudaError_t e = ds::launch_kv_commit(*a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ds_kv_commit launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
+void ds_append_args_default(ds_append_args* a) {
+  if (!a) return;
+  std::memset(a, 0, sizeof(*a));
+  a->kv_layout = DS_KV_NHD;
+}
+
+ds_status ds_compact_append(const ds_append_args* a, void* stream) {
+  REQUIRE(a, DS_ERR_INVALID_ARG, "args is NULL");
+  REQUIRE(a->batch >= 1, DS_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", a->batch);
+  REQUIRE(a->num_kv_heads >= 1, DS_ERR_INVALID_ARG, "num_kv_heads must be >= 1");
+  REQUIRE(a->head_dim == 64 || a->head_dim == 128, DS_ERR_UNSUPPORTED,
+          "head_dim %d (64 or 128)", a->head_dim);
+  REQUIRE(a->page_size >= 1, DS_ERR_INVALID_ARG, "page_size must be >= 1");
+  REQUIRE(a->num_pages >= 1 && a->max_pages >= 1, DS_ERR_INVALID_ARG,
+          "num_pages and max_pages must be >= 1");
+  REQUIRE(a->kv_layout == DS_KV_NHD || a->kv_layout == DS_KV_HND, DS_ERR_INVALID_ARG,
+          "kv_layout %d is not a ds_kv_layout", a->kv_layout);
+  REQUIRE(a->capacity >= 0, DS_ERR_INVALID_ARG, "capacity must be >= 0");
+  REQUIRE(a->rope_base >= 0.f && a->rope_base < 3.0e38f, DS_ERR_INVALID_ARG,
+          "rope_base must be 0 (no rotation) or a finite positive base");
+  REQUIRE(a->src_k && a->src_v && a->page_table && a->from_lens && a->to_lens,
+          DS_ERR_INVALID_ARG, "src_k/src_v/page_table/from_lens/to_lens is NULL");
+  REQUIRE(a->out_k && a->out_v && a->out_positions && a->out_len, DS_ERR_INVALID_ARG,
+          "out_k/out_v/out_positions/out_len is NULL");
+  REQUIRE(aligned16(a->src_k) && aligned16(a->src_v) && aligned16(a->out_k) &&
+              aligned16(a->out_v),
+          DS_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  REQUIRE(a->workspace, DS_ERR_WORKSPACE, "workspace is NULL");
+  REQUIRE(a->workspace_bytes >= ds::kStatusBytes, DS_ERR_WORKSPACE,
+          "workspace_bytes %zu < %zu", a->workspace_bytes, ds::kStatusBytes);
+  cudaError_t e = ds::launch_compact_append(*a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ds_compact_append launch");
   return ok();
 }
 

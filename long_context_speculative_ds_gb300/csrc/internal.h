@@ -58,6 +58,7 @@ cudaError_t launch_accept(const ds_accept_args& a, const AcceptLayout& L,
                           cudaStream_t stream);
 
 cudaError_t launch_kv_commit(const ds_commit_args& a, cudaStream_t stream);
+cudaError_t launch_compact_append(const ds_append_args& a, cudaStream_t stream);
 
 // Sets the message ds_last_error returns on this thread; returns st.
 ds_status set_last_error(ds_status st, const char* msg);

@@ -38,6 +38,8 @@ struct GatherKArgs {
   uint32_t* status;
   float rope_base;           // > 0: rotate K to its local position
   double inv_freq[64];       // rope_base^(-2j/D), j < D/2 (host-computed)
+  const int32_t* from_lens;  // compact append: tokens [from, to) of each sequence
+  const int32_t* to_lens;
 };
 
 constexpr int kSelThreads = 1024;
@@ -171,37 +173,12 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
 }
 
 // One warp per compact row.
-__global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + warp;
-  if (i >= a.capacity) return;
-  int L = __ldg(a.ctx_lens + b);
-  if (L < 0 || (int64_t)L > (int64_t)a.max_pages * a.page_size ||
-      (L + a.chunk_size - 1) / a.chunk_size > a.max_chunks)
-    L = 0;
-  const int ws = max(0, L - a.window);
-  const int n = __ldg(a.out_len + b);
-  int32_t* posrow = a.out_positions + (int64_t)b * a.capacity;
-  if (i >= n) {
-    if (lane == 0) posrow[i] = -1;
-    return;
-  }
-  const int sel_tokens = n - (L - ws);
-  int t;
-  if (i < sel_tokens) {
-    int c = __ldg(a.out_chunk_ids + (int64_t)b * a.top_k + i / a.chunk_size);
-    t = c * a.chunk_size + i % a.chunk_size;
-  } else {
-    t = ws + (i - sel_tokens);
-  }
-  if (lane == 0) posrow[i] = t;
-  int pg = (t >= 0 && t < L) ? __ldg(a.page_table + (int64_t)b * a.max_pages + t / a.page_size) : -1;
-  if (pg < 0 || pg >= a.num_pages) {
-    if (lane == 0) flag(a.status, DS_DEV_BAD_PAGE);
-    pg = -1;
-  }
-  const int off = t % a.page_size;
+// One compact row: source token (page pg, offset off) of every kv head into
+// compact row (b, i), K rotated to local position i when rope_base > 0 (the
+// whole warp calls it; pg < 0 writes zeros).
+DS_DEV void put_row(const GatherKArgs& a, const int b, const int i, const int pg,
+                    const int off) {
+  const int lane = threadIdx.x & 31;
   const int vec_per_head = a.head_dim / 8;            // 16-byte vectors
   const int nvec = a.num_kv_heads * vec_per_head;
   const int64_t drow = ((int64_t)b * a.capacity + i) * a.num_kv_heads * a.head_dim;
@@ -285,6 +262,39 @@ __global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  if (i >= a.capacity) return;
+  int L = __ldg(a.ctx_lens + b);
+  if (L < 0 || (int64_t)L > (int64_t)a.max_pages * a.page_size ||
+      (L + a.chunk_size - 1) / a.chunk_size > a.max_chunks)
+    L = 0;
+  const int ws = max(0, L - a.window);
+  const int n = __ldg(a.out_len + b);
+  int32_t* posrow = a.out_positions + (int64_t)b * a.capacity;
+  if (i >= n) {
+    if (lane == 0) posrow[i] = -1;
+    return;
+  }
+  const int sel_tokens = n - (L - ws);
+  int t;
+  if (i < sel_tokens) {
+    int c = __ldg(a.out_chunk_ids + (int64_t)b * a.top_k + i / a.chunk_size);
+    t = c * a.chunk_size + i % a.chunk_size;
+  } else {
+    t = ws + (i - sel_tokens);
+  }
+  if (lane == 0) posrow[i] = t;
+  int pg = (t >= 0 && t < L) ? __ldg(a.page_table + (int64_t)b * a.max_pages + t / a.page_size) : -1;
+  if (pg < 0 || pg >= a.num_pages) {
+    if (lane == 0) flag(a.status, DS_DEV_BAD_PAGE);
+    pg = -1;
+  }
+  put_row(a, b, i, pg, t % a.page_size);
+}
+
 cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
   GatherKArgs a;
   a.scores = g.scores;
@@ -318,6 +328,79 @@ cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid((g.capacity + 7) / 8, g.batch);
   gather_rows<<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// compact append: between retrievals the compact cache is kept and only the
+// tokens committed since are appended behind its last row (the rolling
+// window grows), K rotated to the appended rows' local positions.  One CTA
+// per sequence, one warp per appended token.
+__global__ void __launch_bounds__(256) compact_append(GatherKArgs a) {
+  __shared__ int s_n0, s_cnt;
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    const int n0 = __ldg(a.out_len + b);
+    const int from = __ldg(a.from_lens + b), to = __ldg(a.to_lens + b);
+    int cnt = to - from;
+    if (from < 0 || cnt < 0 || (int64_t)to > (int64_t)a.max_pages * a.page_size ||
+        n0 < 0 || n0 > a.capacity || (int64_t)n0 + cnt > a.capacity) {
+      flag(a.status, DS_DEV_BAD_LENGTH);
+      cnt = 0;
+    }
+    s_n0 = n0;
+    s_cnt = cnt;
+  }
+  __syncthreads();
+  const int n0 = s_n0, cnt = s_cnt;
+  const int from = __ldg(a.from_lens + b);
+  int32_t* posrow = a.out_positions + (int64_t)b * a.capacity;
+  for (int k = warp; k < cnt; k += 8) {
+    const int t = from + k, i = n0 + k;
+    int pg = __ldg(a.page_table + (int64_t)b * a.max_pages + t / a.page_size);
+    if (pg < 0 || pg >= a.num_pages) {
+      if (lane == 0) flag(a.status, DS_DEV_BAD_PAGE);
+      pg = -1;
+    }
+    if (lane == 0) posrow[i] = t;
+    put_row(a, b, i, pg, t % a.page_size);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && cnt > 0) a.out_len[b] = n0 + cnt;
+}
+
+cudaError_t launch_compact_append(const ds_append_args& g, cudaStream_t stream) {
+  GatherKArgs a{};
+  a.src_k = static_cast<const uint16_t*>(g.src_k);
+  a.src_v = static_cast<const uint16_t*>(g.src_v);
+  a.page_table = g.page_table;
+  a.batch = g.batch;
+  a.num_kv_heads = g.num_kv_heads;
+  a.head_dim = g.head_dim;
+  a.page_size = g.page_size;
+  a.num_pages = g.num_pages;
+  a.max_pages = g.max_pages;
+  a.capacity = g.capacity;
+  const int64_t P = g.page_size, H = g.num_kv_heads, D = g.head_dim;
+  if (g.kv_layout == DS_KV_NHD) {
+    a.page_stride = P * H * D; a.tok_stride = H * D; a.head_stride = D;
+  } else {
+    a.page_stride = H * P * D; a.tok_stride = D; a.head_stride = P * D;
+  }
+  a.out_k = static_cast<uint16_t*>(g.out_k);
+  a.out_v = static_cast<uint16_t*>(g.out_v);
+  a.out_positions = g.out_positions;
+  a.out_len = g.out_len;
+  a.status = static_cast<uint32_t*>(g.workspace);
+  a.rope_base = g.rope_base;
+  for (int j = 0; j < 64; ++j)
+    a.inv_freq[j] = (g.rope_base > 0.f && j < g.head_dim / 2)
+                        ? std::pow((double)g.rope_base, -2.0 * j / g.head_dim)
+                        : 0.0;
+  a.from_lens = g.from_lens;
+  a.to_lens = g.to_lens;
+  compact_append<<<g.batch, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ def test_struct_layouts_and_version(lib):
     assert lib.ds_struct_size(1) == C.sizeof(B.GatherArgs)
     assert lib.ds_struct_size(2) == C.sizeof(B.AcceptArgs)
     assert lib.ds_struct_size(3) == C.sizeof(B.CommitArgs)
+    assert lib.ds_struct_size(4) == C.sizeof(B.AppendArgs)
     assert lib.ds_struct_size(7) == -1
 
 

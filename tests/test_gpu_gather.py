@@ -165,3 +165,67 @@ def test_gather_with_local_rope(layout, head_dim):
         exact += int((ok[b, :n] == exp["out_k"][b, :n]).sum())
         total += ok[b, :n].size
     assert exact >= 0.995 * total, (exact, total)
+
+
+@pytest.mark.parametrize("rope", [0.0, 500000.0])
+def test_compact_append_between_retrievals(rope):
+    """ds_compact_append after a GPU gather: the tokens committed since are
+    appended behind the last row (vllm-diffspec README, "What DiffSpec Does"
+    item 4); compared with the oracle's append of the oracle's gather.  A
+    sequence whose rows would not fit is flagged and left as it was."""
+    wl = synth.tiny_workload(batch=3, chunk_size=32, top_k=3, window=100,
+                             head_dim=128, num_q_heads=8, num_kv_heads=4)
+    # the source pages must cover the appended tokens: contexts as they
+    # will be after the append, retrieval made at the earlier lengths
+    old = [900, 300, 1000]
+    new = [917, 300, 1400]                      # seq 2 overflows the capacity
+    st, inp, mode = H.build_case(wl, layout="NHD", seed=21, ctx_lens=new,
+                                 tree_sizes=(2, 2, 2))
+    step = H.make_step(wl, inp, mode, "NHD")
+    rng = np.random.default_rng(5)
+    scores = rng.random(step.scores.shape).astype(np.float32)
+    _set_scores(step, scores)
+    dev = step.out_k.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    old_t = torch.tensor(old, **i32)
+    cap = step.capacity + 64                    # room for appended rows
+    out_k = torch.zeros(3, cap, 4, 128, dtype=torch.bfloat16, device=dev)
+    out_v = torch.zeros_like(out_k)
+    pos = torch.empty(3, cap, **i32)
+    olen = torch.empty(3, **i32)
+    ids = torch.empty(3, wl.top_k, **i32)
+    ga = B.gather_args(step.scores, old_t, inp.src_k, inp.src_v, inp.page_table,
+                       chunk_size=wl.chunk_size, top_k=wl.top_k, window=wl.window,
+                       out_k=out_k, out_v=out_v, out_positions=pos, out_len=olen,
+                       out_chunk_ids=ids, workspace=step.ws_gather, rope_base=rope)
+    B.ds_chunk_topk_gather(ga)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    aa = B.append_args(inp.src_k, inp.src_v, inp.page_table, old_t,
+                       torch.tensor(new, **i32), out_k=out_k, out_v=out_v,
+                       out_positions=pos, out_len=olen, workspace=ws, rope_base=rope)
+    B.ds_compact_append(aa)
+    torch.cuda.synchronize()
+    assert B.ds_device_status(ws) & B.DS_DEV_BAD_LENGTH          # sequence 2
+    kb, vb = H.bits(inp.src_k), H.bits(inp.src_v)
+    first = ref.gather_compact(kb, vb, st.page_table.numpy(), old, scores.astype(np.float64),
+                               wl.page_size, wl.chunk_size, wl.top_k, wl.window,
+                               cap, rope_base=rope)
+    exp = ref.compact_append(first, kb, vb, st.page_table.numpy(), old, new,
+                             wl.page_size, rope_base=rope)
+    assert olen.cpu().numpy().tolist() == exp["out_len"].tolist()
+    assert exp["out_len"].tolist() == [first["out_len"][0] + 17, first["out_len"][1],
+                                       first["out_len"][2]]
+    np.testing.assert_array_equal(pos.cpu().numpy(), exp["positions"])
+    ok, ov = H.bits(out_k), H.bits(out_v)
+    for b in range(3):
+        n = exp["out_len"][b]
+        np.testing.assert_array_equal(ov[b, :n], exp["out_v"][b, :n])
+        if rope == 0.0:
+            np.testing.assert_array_equal(ok[b, :n], exp["out_k"][b, :n])
+        else:
+            g = ref.bf16_bits_to_f64(ok[b, :n])
+            o = ref.bf16_bits_to_f64(exp["out_k"][b, :n])
+            ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o), 1e-30))) - 7)
+            pair = np.sqrt(o[..., :64] ** 2 + o[..., 64:] ** 2)
+            pair = np.concatenate([pair, pair], axis=-1)
+            assert (np.abs(g - o) <= ulp + 1e-6 * pair).all()
