@@ -89,6 +89,9 @@ ds_status check_verify_sizes(const ds_verify_args* a) {
   const int64_t cache_elems = (int64_t)a->num_pages * a->page_size * a->num_kv_heads *
                               a->head_dim;
   REQUIRE(cache_elems < (int64_t)1 << 40, DS_ERR_UNSUPPORTED, "cache too large");
+  // the HND tensor map addresses (page, kv head) as one coordinate
+  REQUIRE((int64_t)(a->num_pages + 1) * a->num_kv_heads < ((int64_t)1 << 31),
+          DS_ERR_UNSUPPORTED, "num_pages * num_kv_heads must stay below 2^31");
   return DS_OK;
 }
 

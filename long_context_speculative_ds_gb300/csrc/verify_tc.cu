@@ -55,8 +55,8 @@ namespace ds {
 namespace tc {
 
 constexpr int kThreads = 384;
-constexpr uint32_t kHalfBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
-constexpr uint32_t kUnitRowOff = 64 * 128;    // byte offset of key row 64 in a tile half
+// Q tiles: [column half][128 rows x 128 bytes (64 bf16)]
+constexpr uint32_t kHalfBytes = 128 * 128;
 constexpr int kTmemCols = 512;
 
 enum Bar {
@@ -90,6 +90,11 @@ template <int D>
 struct Cfg {
   static constexpr int TB = 128 * D * 2;   // bytes of one 128-row tile
   static constexpr int NH = D / 64;        // 128-byte column halves
+  // K and V tiles: [row group of 8 keys][column half][8 rows x 128 bytes],
+  // so that one page of P keys (P / 8 row groups, all columns) is one
+  // contiguous P * D * 2-byte block that a single TMA box fills; each
+  // 1 KB block of 8 rows x 128 bytes is one 128-byte-swizzle atom
+  static constexpr uint32_t RG = NH * 1024;   // bytes of one row group
   // Q (2 tiles) + K ring (2 slots) + V ring (3 slots) + control block
   static constexpr size_t smem = 7 * TB + sizeof(Ctrl) + 1024;
   static_assert(smem <= 232448, "dynamic shared memory above the 227 KB a block can have");
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ loader
       const int P = a.plan.page_size;
       const int npg = kTileKeys / P;
-      const int nops = npg * NH;                  // TMA boxes per tile per tensor
+      const int nops = npg;                       // TMA boxes (one per page) per tile
       const int32_t* ptab = a.page_table + (int64_t)p.b * a.plan.max_pages;
       if (lane == 0) {
         prefetch_tmap(&tm_q);
@@ -479,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pg = 0;
         bool lane_tma = false;
         if (lane < nops) {
-          const int ps = slot0 + (lane / NH) * P;
+          const int ps = slot0 + lane * P;
           if (ps + P <= valid_end) {
             pg = __ldg(ptab + ps / P);
             if (pg < 0 || pg >= a.num_pages) {
@@ -500,19 +505,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         if (lane == 0) {
           if (partial)
-            mbar_expect_tx(full, __popc(tma_lanes) * P * 128);
+            mbar_expect_tx(full, __popc(tma_lanes) * P * D * 2);
           else
             mbar_arrive_expect_tx(full, TB);
         }
         __syncwarp();
         if (lane_tma) {
-          const int pp = lane / NH, hf = lane % NH;
-          const uint32_t d = dst + hf * kHalfBytes + pp * P * 128;
+          // coordinates (column, row in group, column half, row group, page);
+          // the map folds the kv head into the half axis (NHD) or the page
+          // axis (HND)
+          const uint32_t d = dst + lane * P * D * 2;
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
           if (hnd)
-            tma_load_4d(d, m, full, hf * 64, 0, kvh, pg);
+            tma_load_5d(d, m, full, 0, 0, 0, 0, pg * a.plan.num_kv_heads + kvh);
           else
-            tma_load_4d(d, m, full, hf * 64, kvh, 0, pg);
+            tma_load_5d(d, m, full, 0, 0, kvh * NH, 0, pg);
         }
         if (partial) {
           // the one page with ps < valid_end < ps + P: plain 16-byte loads,
@@ -547,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (e < nelem) {
                 const int kk = pidx * P + e / VPR, c = e % VPR;
                 const int hf = c >> 3, c8 = c & 7;
-                const uint32_t d = dst + hf * kHalfBytes + kk * 128 + ((c8 ^ (kk & 7)) << 4);
+                const uint32_t d = dst + (kk >> 3) * Cfg<D>::RG + hf * 1024 + (kk & 7) * 128 +
+                                   ((c8 ^ (kk & 7)) << 4);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(x[r].x),
                              "r"(x[r].y), "r"(x[r].z), "r"(x[r].w)
                              : "memory");
@@ -593,9 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 256 KB, so the add never carries into the neighbouring fields).
         const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);
         const uint64_t qb = (row_mode && g == 1) ? qd0 + (TB >> 4) : qd0;   // this group's Q
-        const uint64_t kd0 = sdesc_sw128(sK, 16, 1024);
-        const uint64_t kd2 = sdesc_sw128(sQ + TB, 16, 1024);      // K slot 2 (key mode)
-        const uint64_t vd0 = sdesc_sw128(sV, kHalfBytes, 1024);
+        constexpr uint32_t RG = Cfg<D>::RG;
+        // K: K-major, 8-row groups RG bytes apart.  V: MN-major, the two
+        // 64-column halves 1 KB apart (LBO), 8-key groups RG apart (SBO).
+        const uint64_t kd0 = sdesc_sw128(sK, 16, RG);
+        const uint64_t kd2 = sdesc_sw128(sQ + TB, 16, RG);        // K slot 2 (key mode)
+        const uint64_t vd0 = sdesc_sw128(sV, 1024, RG);
         const uint32_t tG = tmem + (uint32_t)(256 * g);
         // users of each K and V tile: both groups in row mode, one in key
         // mode (which then releases the slot with two commits)
@@ -609,21 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto qk = [&](int t, int h) {
           const int ks = kslot_of(t);
           const uint64_t kb = (ks < 2 ? kd0 + (uint64_t)(ks * (TB >> 4)) : kd2) +
-                              (uint64_t)(h * (kUnitRowOff >> 4));
+                              (uint64_t)(h * ((8 * RG) >> 4));
           const uint32_t d = tG + (uint32_t)(64 * h);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-            mma_ss(d, qb + off, kb + off, idesc_qk, kk > 0);
+            const uint32_t qoff = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            const uint32_t koff = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            mma_ss(d, qb + qoff, kb + koff, idesc_qk, kk > 0);
           }
         };
         // O += P(half h) V(keys 64 h .. 64 h + 63)
         auto pv = [&](int t, int h, bool acc) {
-          const uint64_t vb = vd0 + (uint64_t)((t % 3) * (TB >> 4) + h * (kUnitRowOff >> 4));
+          const uint64_t vb = vd0 + (uint64_t)((t % 3) * (TB >> 4) + h * ((8 * RG) >> 4));
           const uint32_t pa = tG + (uint32_t)(64 * h);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tG + 128, pa + kk * 8, vb + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+            mma_ts(tG + 128, pa + kk * 8, vb + (uint64_t)(kk * ((2 * RG) >> 4)), idesc_pv,
                    (acc || kk > 0) ? 1u : 0u);
         };
         const int wi = g == 0 ? 1 : 4;   // this issuer's slot in ctrl->where
@@ -837,7 +849,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -855,24 +867,31 @@ cudaError_t launch_tc(const VerifyKArgs& k, const ds_verify_args& a, const Verif
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
     if (!encode(&tq, a.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // K and V: one box is one page of one kv head, all columns, landing as
+  // [row group of 8][column half][8 rows x 128 bytes].  Axes: column (64),
+  // row in group (8), column half, row group (P / 8), page.  NHD
+  // [pages, P, H, D]: the kv head is folded into the half axis (halves of
+  // consecutive heads are 128 bytes apart).  HND [pages, H, P, D]: the kv
+  // head is folded into the page axis (coordinate page * H + head).
   const bool hnd = a.kv_layout == DS_KV_HND;
-  cuuint64_t dims[4], strides[3];
-  cuuint32_t box[4];
-  if (!hnd) {   // [pages, P, H, D]: dims (D, H, P, pages)
-    cuuint64_t d[4] = {(cuuint64_t)D, H, P, NP};
-    cuuint64_t s[3] = {(cuuint64_t)D * 2, H * D * 2, P * H * D * 2};
-    cuuint32_t b[4] = {64, 1, (cuuint32_t)P, 1};
-    for (int i = 0; i < 4; ++i) { dims[i] = d[i]; box[i] = b[i]; }
-    for (int i = 0; i < 3; ++i) strides[i] = s[i];
-  } else {      // [pages, H, P, D]: dims (D, P, H, pages)
-    cuuint64_t d[4] = {(cuuint64_t)D, P, H, NP};
-    cuuint64_t s[3] = {(cuuint64_t)D * 2, P * D * 2, H * P * D * 2};
-    cuuint32_t b[4] = {64, (cuuint32_t)P, 1, 1};
-    for (int i = 0; i < 4; ++i) { dims[i] = d[i]; box[i] = b[i]; }
-    for (int i = 0; i < 3; ++i) strides[i] = s[i];
+  constexpr cuuint64_t NH = D / 64;
+  cuuint64_t dims[5], strides[4];
+  const cuuint32_t box[5] = {64, 8, (cuuint32_t)NH, (cuuint32_t)(P / 8), 1};
+  if (!hnd) {
+    const cuuint64_t row = H * D * 2;
+    const cuuint64_t d[5] = {64, 8, NH * H, P / 8, NP};
+    const cuuint64_t s[4] = {row, 128, 8 * row, P * row};
+    for (int i = 0; i < 5; ++i) dims[i] = d[i];
+    for (int i = 0; i < 4; ++i) strides[i] = s[i];
+  } else {
+    const cuuint64_t row = D * 2;
+    const cuuint64_t d[5] = {64, 8, NH, P / 8, H * NP};
+    const cuuint64_t s[4] = {row, 128, 8 * row, P * row};
+    for (int i = 0; i < 5; ++i) dims[i] = d[i];
+    for (int i = 0; i < 4; ++i) strides[i] = s[i];
   }
-  if (!encode(&tk, a.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
-  if (!encode(&tv, a.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  if (!encode(&tk, a.k_cache, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  if (!encode(&tv, a.v_cache, 5, dims, strides, box)) return cudaErrorInvalidValue;
   const size_t smem = tc::Cfg<D>::smem;
   static bool attr = false;
   if (!attr) {
