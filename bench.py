@@ -35,6 +35,7 @@ METRIC = ("µs/verify-step/layer and KV GB/s (% HBM peak) at 128K ctx, "
 UNIT = "us/verify-step/layer"
 DEFAULT_WORKLOAD = "llama8b-128k-32l"
 FALLBACK_HBM_GBS = 6800.0
+EV_EVERY = 4          # split-pass events bracket every 4th layer's launch
 
 
 def _peaks():
@@ -217,6 +218,8 @@ def _config(wl, st, kv_layout="NHD"):
             "chunk_size": wl.chunk_size, "top_k": wl.top_k,
             "window": wl.window, "vocab": wl.vocab, "accept": wl.accept,
             "rope_base": wl.rope_base, "kv_commit": True,
+            "split_events": f"split pass of layers {EV_EVERY - 1}, "
+                            f"{2 * EV_EVERY - 1}, ... (every {EV_EVERY}th)",
             "l2": "inputs larger than L2: every layer has its own "
                   f"{_kv_bytes(wl, st) / 1e6:.0f} MB K/V cache"}
 
@@ -307,23 +310,29 @@ def run_ours(args, wl, rank, world, local_rank):
                       window=wl.window, accept_mode=mode,
                       kv_layout=args.kv_layout, with_commit=True,
                       rope_base=wl.rope_base)
-    # per-layer events around the split-pass kernel
-    n_ev = args.steps * wl.layers
+    # events around the split-pass kernel of every EV_EVERY-th layer
+    # (layers EV_EVERY - 1, 2 EV_EVERY - 1, ...; never layer 0, whose split
+    # follows the step's gather, acceptance and commit rather than another
+    # layer): each event pair sits between two kernels of the step and
+    # costs it a few microseconds, so only a sample of the launches is
+    # bracketed
+    every = min(EV_EVERY, wl.layers)
+    sampled = [(s_, l) for s_ in range(args.steps) for l in range(wl.layers)
+               if l % every == every - 1]
     evs = [(torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+            torch.cuda.Event(enable_timing=True)) for _ in sampled]
     for e_a, e_b in evs:      # torch creates the CUDA event on first record
         e_a.record()
         e_b.record()
     torch.cuda.synchronize()
-    prof_args = []
-    for i in range(n_ev):
-        l = i % wl.layers
-        prof_args.append(binding.verify_args(
+    prof_args = {}
+    for (s_, l), ev in zip(sampled, evs):
+        prof_args[(s_, l)] = binding.verify_args(
             inp.q[l], inp.k_cache[l], inp.v_cache[l], inp.page_table,
             inp.ctx_lens, inp.tree_offsets, inp.parents,
             chunk_size=wl.chunk_size, out=step.out[l],
             chunk_scores=step.scores, workspace=step.ws_verify,
-            kv_layout=args.kv_layout, accumulate=l > 0, prof_events=evs[i]))
+            kv_layout=args.kv_layout, accumulate=l > 0, prof_events=ev)
 
     def barrier():
         if world > 1:
@@ -343,7 +352,7 @@ def run_ours(args, wl, rank, world, local_rank):
     e0.record()
     for s in range(args.steps):
         for l in range(wl.layers):
-            binding.ds_verify_attn(prof_args[s * wl.layers + l])
+            binding.ds_verify_attn(prof_args.get((s, l), step.verify_args[l]))
         step.gather()
         step.accept()
         step.commit()

@@ -21,17 +21,24 @@
 
 #include "dev_common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 #include "verify_common.cuh"
 
 namespace ds {
 
 // ---------------------------------------------------------------------------
-// combine: one warp per (sequence, kv head, row group, row).  The split
-// log2-sum-exps are read lane-parallel; split outputs are accumulated eight
-// splits at a time so that eight 16-byte loads per lane are in flight.
+// combine: one warp per (sequence, kv head, row group, row).  Both round
+// trips of a row are issued together: the outputs of its first kCombBatch
+// splits (lane-parallel over columns) and the split log2-sum-exps
+// (lane-parallel over splits); the weights 2^{lse_s - lse} are then
+// broadcast from the lane that holds split s.
+constexpr int kCombBatch = 24;
+
 template <int D>
 __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
   __shared__ Plan s_plan;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   const int per_b = a.plan.num_kv_heads * a.plan.rg_max;
   const int b = blockIdx.x / per_b;
   const int h = (blockIdx.x / a.plan.rg_max) % a.plan.num_kv_heads;
@@ -55,48 +62,63 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
   const int base = sq.item_base + (h * sq.rg + rgi) * sq.splits;
   const int ns = sq.splits;
   const float* lp = a.lse_part + (int64_t)base * kRowsPerGroup + r;
+  constexpr int E = D / 32;   // floats per lane (4 or 2)
+  const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
+  const int64_t sstride = (int64_t)kRowsPerGroup * D;
 
-  float mx = -CUDART_INF_F;
-  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * kRowsPerGroup));
+  auto load_o = [&](int s, float (&x)[E]) {
+    const float* op = op0 + (int64_t)s * sstride;
+    if constexpr (E == 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(op));
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(op));
+      x[0] = v.x; x[1] = v.y;
+    }
+  };
+  float x[kCombBatch][E];
+#pragma unroll
+  for (int k = 0; k < kCombBatch; ++k) {
+    if (k < ns) load_o(k, x[k]);
+  }
+  const float l0 = lane < ns ? __ldg(lp + (int64_t)lane * kRowsPerGroup) : -CUDART_INF_F;
+  float mx = l0;
+  for (int s = lane + 32; s < ns; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * kRowsPerGroup));
   mx = warp_max(mx);
-  float sum = 0.f;
-  for (int s = lane; s < ns; s += 32) sum += exp2f(__ldg(lp + (int64_t)s * kRowsPerGroup) - mx);
+  float sum = lane < ns ? exp2f(l0 - mx) : 0.f;
+  for (int s = lane + 32; s < ns; s += 32) sum += exp2f(__ldg(lp + (int64_t)s * kRowsPerGroup) - mx);
   sum = warp_sum(sum);
   const float lse = mx + log2f(sum);
 
-  constexpr int E = D / 32;   // floats per lane (4 or 2)
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
-  const int64_t sstride = (int64_t)kRowsPerGroup * D;
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    // weight of split s0 + lane, broadcast below
-    const float wl = (s0 + lane < ns)
-                         ? exp2f(__ldg(lp + (int64_t)(s0 + lane) * kRowsPerGroup) - lse) : 0.f;
-    const int cnt = min(32, ns - s0);
-    for (int k0 = 0; k0 < cnt; k0 += 8) {
-      float x[8][E];
+  // weight of split `lane` (of the first 32), broadcast below
+  const float w0 = lane < ns ? exp2f(l0 - lse) : 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k0 + k < cnt) {
-          const float* op = op0 + (int64_t)(s0 + k0 + k) * sstride;
-          if constexpr (E == 4) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(op));
-            x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
-          } else {
-            const float2 v = __ldg(reinterpret_cast<const float2*>(op));
-            x[k][0] = v.x; x[k][1] = v.y;
-          }
-        }
-      }
+  for (int k = 0; k < kCombBatch; ++k) {
+    const float w = __shfl_sync(0xffffffffu, w0, k);
+    if (k < ns && w != 0.f) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
-        if (k0 + k < cnt && w != 0.f) {
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
+    }
+  }
+  // more than kCombBatch splits: the rest eight at a time
+  for (int s0 = kCombBatch; s0 < ns; s0 += 8) {
+    float y[8][E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
-        }
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k < ns) load_o(s0 + k, y[k]);
+    }
+    const float wl = (s0 + (lane & 7) < ns)
+                         ? exp2f(__ldg(lp + (int64_t)(s0 + (lane & 7)) * kRowsPerGroup) - lse)
+                         : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wl, k);
+      if (s0 + k < ns && w != 0.f) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, y[k][e], acc[e]);
       }
     }
   }
@@ -116,43 +138,63 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// finalize: one CTA per (chunk, sequence).  Warp w sums the rows of kv heads
-// / row groups w, w + 8, ...; each lane keeps eight loads of chunk mass and
-// eight of row log2-sum-exp in flight.
-__global__ void __launch_bounds__(256) chunk_finalize(VerifyKArgs a) {
-  __shared__ float s_part[8];
+// finalize: one warp per (chunk, sequence), four chunks per CTA.  Lane i
+// covers rows 4i .. 4i + 3 and 128 + 4i .. 128 + 4i + 3 of every (kv head,
+// row group) with 16-byte loads; four (kv head, row group) combinations are
+// loaded per round, 16 loads in flight per lane.
+constexpr int kFinWarps = 4;
+
+__global__ void __launch_bounds__(32 * kFinWarps) chunk_finalize(VerifyKArgs a) {
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   const int b = blockIdx.y;
-  const int c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kFinWarps + warp;
   const SeqPlan sq = seq_sizes(a.plan, b, false);
   const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
   if (c >= n_ch) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static_assert(kRowsPerGroup == 256, "two 128-row halves of four rows per lane");
   float sum = 0.f;
   const int combos = a.plan.num_kv_heads * sq.rg;
-  for (int cb = warp; cb < combos; cb += 8) {
-    const int h = cb / sq.rg, rgi = cb % sq.rg;
-    const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
-    const int64_t hb = ((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi;
-    const float* cl = a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup;
-    const float* rl = a.row_lse + hb * kRowsPerGroup;
-    float v[8], w[8];
+  for (int cb0 = 0; cb0 < combos; cb0 += 4) {
+    float4 v[4][2], w[4][2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int r = lane + 32 * k;
-      v[k] = r < rows_here ? __ldg(cl + r) : -CUDART_INF_F;
-      w[k] = r < rows_here ? __ldg(rl + r) : 0.f;
+    for (int k = 0; k < 4; ++k) {
+      const int cb = cb0 + k;
+      if (cb < combos) {
+        const int h = cb / sq.rg, rgi = cb % sq.rg;
+        const int64_t hb = ((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi;
+        const float4* cl = reinterpret_cast<const float4*>(
+            a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup);
+        const float4* rl = reinterpret_cast<const float4*>(a.row_lse + hb * kRowsPerGroup);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          v[k][q] = __ldg(cl + lane + 32 * q);
+          w[k][q] = __ldg(rl + lane + 32 * q);
+        }
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sum += exp2f(v[k] - w[k]);
+    for (int k = 0; k < 4; ++k) {
+      const int cb = cb0 + k;
+      if (cb < combos) {
+        const int rows_here = min(kRowsPerGroup, sq.rows - (cb % sq.rg) * kRowsPerGroup);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int r0 = 4 * lane + 128 * q;
+          const float vv[4] = {v[k][q].x, v[k][q].y, v[k][q].z, v[k][q].w};
+          const float ww[4] = {w[k][q].x, w[k][q].y, w[k][q].z, w[k][q].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (r0 + e < rows_here) sum += exp2f(vv[e] - ww[e]);
+        }
+      }
+    }
   }
   sum = warp_sum(sum);
-  if (lane == 0) s_part[warp] = sum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int i = 0; i < 8; ++i) t += s_part[i];
+  if (lane == 0) {
     float* dst = a.scores + (int64_t)b * a.plan.max_chunks + c;
-    *dst = a.accumulate ? *dst + t : t;
+    *dst = a.accumulate ? *dst + sum : sum;
   }
 }
 
@@ -170,13 +212,11 @@ static cudaError_t launch_d(const VerifyKArgs& k, const ds_verify_args& a,
   if (e != cudaSuccess) return e;
   if (ev1) cudaEventRecord(ev1, stream);
   dim3 gc(batch * k.plan.num_kv_heads * L.rg_max, kRowsPerGroup / 8);
-  verify_combine<D><<<gc, 256, 0, stream>>>(k);
-  e = cudaGetLastError();
+  e = launch_dependent(verify_combine<D>, gc, dim3(256), 0, stream, k);
   if (e != cudaSuccess) return e;
   if (k.plan.max_chunks > 0) {
-    dim3 gf(k.plan.max_chunks, batch);
-    chunk_finalize<<<gf, 256, 0, stream>>>(k);
-    e = cudaGetLastError();
+    dim3 gf((k.plan.max_chunks + kFinWarps - 1) / kFinWarps, batch);
+    e = launch_dependent(chunk_finalize, gf, dim3(32 * kFinWarps), 0, stream, k);
   }
   return e;
 }

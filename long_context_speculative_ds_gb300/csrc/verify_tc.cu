@@ -48,6 +48,7 @@
 
 #include "dev_common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 #include "tc_ptx.cuh"
 #include "verify_common.cuh"
 
@@ -302,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using namespace ptx;
   constexpr int TB = Cfg<D>::TB;
   constexpr int NH = Cfg<D>::NH;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -900,8 +903,8 @@ cudaError_t launch_tc(const VerifyKArgs& k, const ds_verify_args& a, const Verif
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  tc::verify_split_tc<D><<<L.max_items, tc::kThreads, smem, stream>>>(tq, tk, tv, k, hnd ? 1 : 0);
-  return cudaGetLastError();
+  return launch_dependent(tc::verify_split_tc<D>, dim3(L.max_items), dim3(tc::kThreads), smem,
+                          stream, tq, tk, tv, k, hnd ? 1 : 0);
 }
 
 }  // namespace
