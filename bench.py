@@ -67,8 +67,12 @@ def _q_bytes(wl, st):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+    """nvidia-smi clock / throttle-reason samples during the timed region:
+    the sampler is started (and its first sample awaited) before the region,
+    and only samples stamped inside the region's host-clock window are kept;
+    when the region is shorter than the sampling period and none falls
+    inside, the sample nearest to it is reported with samples = 0."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,"
@@ -89,7 +93,15 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def wait_ready(self, timeout_s: float = 3.0):
+        """Blocks until nvidia-smi has written its first sample."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and time.time() < t_end:
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.01)
+
+    def stop(self, t0: float = None, t1: float = None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -98,27 +110,41 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(lines, t0, t1)
+
+
+def parse_clock_samples(lines, t0=None, t1=None):
+    """Summary of nvidia-smi csv lines (timestamp first) within [t0, t1]
+    (host epoch seconds); the nearest sample when none is inside."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap"]
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append((ts, float(parts[2]), float(parts[3]),
+                         [n for n, v in zip(names, parts[6:10])
+                          if v.lower().startswith("active")]))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    inside = rows if t0 is None else [r for r in rows if t0 <= r[0] <= t1]
+    n_inside = len(inside)
+    if not inside:
+        mid = 0.5 * (t0 + t1)
+        inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+    reasons = sorted({n for r in inside for n in r[3]})
+    return {"sm_mhz": statistics.median(r[1] for r in inside),
+            "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+            "samples": n_inside}
 
 
 # ---------------------------------------------------------------------------
@@ -344,11 +370,13 @@ def run_ours(args, wl, rank, world, local_rank):
     assert step.device_status() == 0
 
     sampler = ClockSampler(local_rank)
+    sampler.start()
+    sampler.wait_ready()
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    t_region0 = time.time()
     e0.record()
     for s in range(args.steps):
         for l in range(wl.layers):
@@ -358,8 +386,9 @@ def run_ours(args, wl, rank, world, local_rank):
         step.commit()
     e1.record()
     torch.cuda.synchronize()
+    t_region1 = time.time()
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_region0, t_region1)
     ms = e0.elapsed_time(e1) / args.steps
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if world > 1:
@@ -401,6 +430,26 @@ def run_ours(args, wl, rank, world, local_rank):
     assert binding.ds_device_status(c_ws) == 0
     commit_us = c0.elapsed_time(c1) * 1e3 / reps
     commit_bytes = sum(n_acc) * wl.num_kv_heads * wl.head_dim * 2 * 2 * 2 * wl.layers
+
+    # retrieval (top-k + gather) and acceptance alone, each over its own
+    # algorithmic bytes: the compact tokens' K and V read and written; the
+    # logits read (target, plus draft for rejection)
+    def _alone(fn):
+        fn()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(reps):
+            fn()
+        a1.record()
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) * 1e3 / reps
+    gather_us = _alone(step.gather)
+    accept_us = _alone(step.accept)
+    assert step.device_status() == 0
+    compact_tokens = int(step.out_len.sum().item())
+    gather_bytes = compact_tokens * wl.num_kv_heads * wl.head_dim * 2 * 2 * 2
+    accept_bytes = st.n_nodes * wl.vocab * 4 * (2 if mode == "reject" else 1)
 
     # compact append between retrievals: the root and the accepted path
     # (1 + n tokens) appended behind a compact cache with room for them
@@ -471,6 +520,13 @@ def run_ours(args, wl, rank, world, local_rank):
                 "note": "committed and tree K/V stay resident (model state);"
                         " per-step Q, tree, page table, logits, uniforms in,"
                         " path/bonus/chunk ids out"},
+        "gather": {"us": round(gather_us, 2), "compact_tokens": compact_tokens,
+                   "algorithmic_bytes": gather_bytes,
+                   "gbs": round(gather_bytes / (gather_us * 1e-6) / 1e9, 1),
+                   "rope": wl.rope_base > 0},
+        "accept": {"us": round(accept_us, 2), "mode": mode,
+                   "algorithmic_bytes": accept_bytes,
+                   "gbs": round(accept_bytes / (accept_us * 1e-6) / 1e9, 1)},
         "kv_commit": {"us": round(commit_us, 2), "accepted": n_acc,
                       "algorithmic_bytes": commit_bytes,
                       "gbs": round(commit_bytes / (commit_us * 1e-6) / 1e9, 1)
@@ -493,7 +549,7 @@ def run_ours(args, wl, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

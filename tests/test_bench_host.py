@@ -1,0 +1,36 @@
+"""Host logic of bench.py that needs no GPU: the clock-sample window filter
+(samples are kept only when stamped inside the timed region; the nearest
+one stands in, with samples = 0, when the region is shorter than the
+sampling period) and throttle-reason collection."""
+import datetime
+
+import bench
+
+
+def _line(t, sm, mx, power_cap="Not Active", thermal="Not Active"):
+    ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return (f"{ts}, 0, {sm}, {mx}, 900.00, 0x0000000000000000, Not Active, "
+            f"{thermal}, Not Active, {power_cap}\n")
+
+
+def test_window_keeps_only_inside_samples():
+    t = 1_800_000_000.0
+    lines = [_line(t, 1000, 2070), _line(t + 0.1, 2070, 2070),
+             _line(t + 0.15, 2050, 2070, power_cap="Active"), _line(t + 0.5, 900, 2070)]
+    got = bench.parse_clock_samples(lines, t + 0.05, t + 0.2)
+    assert got["samples"] == 2
+    assert got["sm_mhz"] == 2060
+    assert got["sm_max_mhz"] == 2070
+    assert got["reasons"] == ["sw_power_cap"]
+
+
+def test_short_region_takes_nearest_sample():
+    t = 1_800_000_000.0
+    lines = [_line(t, 1500, 2070), _line(t + 0.05, 2070, 2070, thermal="Active")]
+    got = bench.parse_clock_samples(lines, t + 0.04, t + 0.045)
+    assert got["samples"] == 0
+    assert got["sm_mhz"] == 2070 and got["reasons"] == ["hw_thermal_slowdown"]
+
+
+def test_garbage_lines_ignored():
+    assert bench.parse_clock_samples(["", "bad line\n"], 0.0, 1.0) is None
