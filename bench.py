@@ -267,8 +267,9 @@ def _traffic_for(src_path: str):
 # ---------------------------------------------------------------------------
 
 def _end_to_end(step, inp, args, world, dev, barrier):
-    """Per step: copy the step's inputs from pinned host memory, run the
-    step through the library, read the results back; wall-clock timed."""
+    """Per step: copy the step's inputs from pinned host memory (on a side
+    stream, overlapping the verify of earlier layers), run the step through
+    the library, read the results back; wall-clock timed."""
     import torch
     from long_context_speculative_ds_gb300.step import StepInputs
     pin = lambda t: None if t is None else t.cpu().pin_memory()
@@ -283,17 +284,13 @@ def _end_to_end(step, inp, args, world, dev, barrier):
                 for n in ("out_path", "out_n", "out_bonus", "out_chunk_ids",
                           "out_len")}
     for _ in range(max(1, min(args.warmup, 2))):
-        step.upload(host)
-        step.run()
-        step.download(host_out)
+        step.run_from_host(host, host_out)
     torch.cuda.synchronize()
     barrier()
     h2d = d2h = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        h2d = step.upload(host)
-        step.run()
-        d2h = step.download(host_out)
+        h2d, d2h = step.run_from_host(host, host_out)
         torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     if world > 1:

@@ -180,6 +180,56 @@ class VerifyStep:
             n += src.numel() * src.element_size()
         return n
 
+    def run_from_host(self, host: "StepInputs", host_out: dict):
+        """One step end to end from pinned host inputs, with the copies on a
+        side stream: the tree, then each layer's Q, then the logits, each
+        behind an event that only the kernels reading it wait on, so the
+        copies of later layers and of the logits overlap the verify of
+        earlier layers.  The side stream first waits for the current stream
+        (the previous step's kernels may still read these buffers).
+        Returns (host-to-device bytes, device-to-host bytes)."""
+        comp = torch.cuda.current_stream()
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream()
+            self._ev_tree = torch.cuda.Event()
+            self._ev_q = [torch.cuda.Event() for _ in range(self.layers)]
+            self._ev_acc = torch.cuda.Event()
+        cp = self._copy_stream
+        cp.wait_stream(comp)
+        d = self.inp
+        n = 0
+
+        def put(dst, src):
+            nonlocal n
+            dst.copy_(src, non_blocking=True)
+            n += src.numel() * src.element_size()
+
+        with torch.cuda.stream(cp):
+            for dst, src in ((d.page_table, host.page_table), (d.ctx_lens, host.ctx_lens),
+                             (d.tree_offsets, host.tree_offsets), (d.parents, host.parents)):
+                put(dst, src)
+            self._ev_tree.record(cp)
+            for l in range(self.layers):
+                put(d.q[l], host.q[l])
+                self._ev_q[l].record(cp)
+            put(d.target_logits, host.target_logits)
+            put(d.draft_tokens, host.draft_tokens)
+            if d.draft_logits is not None:
+                put(d.draft_logits, host.draft_logits)
+            if d.uniforms is not None:
+                put(d.uniforms, host.uniforms)
+            self._ev_acc.record(cp)
+        comp.wait_event(self._ev_tree)
+        for l in range(self.layers):
+            comp.wait_event(self._ev_q[l])
+            self.verify_layer(l)
+        self.gather()
+        comp.wait_event(self._ev_acc)
+        self.accept()
+        if self.with_commit:
+            self.commit()
+        return n, self.download(host_out)
+
     def download(self, host_out: dict):
         """Copy the step's small results (accepted path, count, bonus, chosen
         chunks, compact length) to pinned host tensors."""
