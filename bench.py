@@ -258,10 +258,21 @@ def _traffic_for(src_path: str):
         return None
     with open(p) as f:
         d = json.load(f)
-    sha = hashlib.sha256(open(src_path, "rb").read()).hexdigest()
-    if d.get("source_sha256") != sha:
+    if d.get("source_code_sha256") != code_sha256(src_path):
         return None
     return d.get("dram_bytes_per_launch_full_size")
+
+
+def code_sha256(src_path: str) -> str:
+    """sha256 of a C++/CUDA source with comments and blank space removed, so
+    that edits to comments alone do not invalidate counters taken from it
+    (string literals in the kernel sources hold no comment markers)."""
+    import re
+    text = open(src_path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = re.sub(r"\s+", " ", text).strip()
+    return hashlib.sha256(text.encode()).hexdigest()
 
 
 # ---------------------------------------------------------------------------

@@ -8,9 +8,9 @@
 // stream order.  What the launch attribute buys is that the dependent grid
 // is already scheduled when that happens (its launch latency overlaps the
 // tail of the preceding grid); each kernel signals launch_dependents as soon
-// as it starts.  A kernel launched without the attribute (or preceded by a
-// kernel that never signals) sees griddepcontrol.wait return at once / the
-// dependent launched at the preceding grid's completion.
+// as it starts.  In a kernel launched without the attribute
+// griddepcontrol.wait returns at once; a dependent of a kernel that never
+// signals is launched when that kernel completes.
 #pragma once
 #include <cuda_runtime.h>
 

@@ -4,10 +4,13 @@
 // One CTA per work item (sequence, kv head, row group of up to 256 query
 // rows, contiguous range of 128-key tiles), 12 warps:
 //   warp 0      loader: Q once, then K and V tiles into shared-memory rings.
-//               Tiles wholly inside the committed context arrive by TMA, one
-//               box per (page, 64-column half); the one or two tiles that
-//               hold tree slots or the end of the sequence are copied with
-//               plain loads so that slots past the sequence end read as zero.
+//               Pages wholly inside the sequence arrive by TMA, one box per
+//               page (all columns of one kv head: a 5-D tensor map lands it
+//               as [8-row group][64-column half][8 rows x 128 B], whole
+//               128-byte-swizzle atoms); the one page that holds the
+//               sequence end is copied with plain loads so that slots past
+//               the end read as zero, and pages wholly past the end get an
+//               out-of-range coordinate (TMA fills zeros).
 //   warp 1      tensor-memory allocator.
 //   warps 2, 3  MMA issuers of softmax groups 0 and 1 (one thread each).
 //   warps 4-7   softmax group 0, warps 8-11 softmax group 1 (each a whole
