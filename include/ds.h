@@ -175,7 +175,11 @@ ds_status ds_verify_attn_workspace_size(const ds_verify_args* args,
 
 /* Enqueue the verify step.  Output `out` and `chunk_scores` are complete
  * when the work on `stream` completes.  The workspace must not be shared by
- * calls that may overlap on the GPU. */
+ * calls that may overlap on the GPU.  Its three kernels are launched as
+ * programmatic dependents of the preceding work on `stream` (each waits for
+ * that work to complete before it reads or writes memory, so ordering is
+ * that of the stream; only launch latency overlaps); an event recorded
+ * between two calls (for example `prof_event_*`) simply ends that overlap. */
 ds_status ds_verify_attn(const ds_verify_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ *
