@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   DS_OK = 0,
   DS_ERR_INVALID_ARG = 1,  /* a NULL pointer, negative size, bad enum, ...  */
-  DS_ERR_UNSUPPORTED = 2,  /* a valid value this build refuses by name      */
+  DS_ERR_UNSUPPORTED = 2,  /* a valid value the library does not support    */
   DS_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed   */
   DS_ERR_TIMEOUT = 4,      /* reserved: a bounded device-side wait gave up  */
   DS_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small    */
