@@ -130,3 +130,72 @@ def test_gather_and_accept_refusals(lib):
     assert "draft_logits" in lib.ds_last_error().decode()
     assert lib.ds_accept_workspace_size(C.byref(a), C.byref(n)) == B.DS_OK
     assert n.value >= 256 + 4 * 48
+
+
+def _commit_args(**kw):
+    a = B.CommitArgs()
+    B.load().ds_commit_args_default(C.byref(a))
+    ptrs = (C.c_void_p * 2)(256, 512)
+    a.k_caches = C.cast(ptrs, C.POINTER(C.c_void_p))
+    a.v_caches = C.cast(ptrs, C.POINTER(C.c_void_p))
+    base = dict(num_layers=2, batch=1, num_kv_heads=8, head_dim=128, page_size=16,
+                num_pages=10, max_pages=4, page_table=16, ctx_lens=32,
+                tree_offsets=48, path=64, n_accepted=80, new_ctx_lens=96,
+                workspace=4096, workspace_bytes=256)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return a, ptrs
+
+
+@pytest.mark.parametrize("field,value,status,word", [
+    ("num_layers", 0, B.DS_ERR_UNSUPPORTED, "num_layers"),
+    ("num_layers", 129, B.DS_ERR_UNSUPPORTED, "num_layers"),
+    ("head_dim", 96, B.DS_ERR_UNSUPPORTED, "head_dim"),
+    ("page_size", 24, B.DS_ERR_UNSUPPORTED, "page_size"),
+    ("batch", 0, B.DS_ERR_INVALID_ARG, "batch"),
+    ("kv_layout", 3, B.DS_ERR_INVALID_ARG, "kv_layout"),
+    ("new_ctx_lens", 32, B.DS_ERR_INVALID_ARG, "alias"),
+    ("path", None, B.DS_ERR_INVALID_ARG, "is NULL"),
+    ("workspace_bytes", 8, B.DS_ERR_WORKSPACE, "workspace_bytes"),
+])
+def test_commit_refuses_by_name(lib, field, value, status, word):
+    a, keep = _commit_args(**{field: value})
+    st = lib.ds_kv_commit(C.byref(a), None)
+    assert st == status and word in lib.ds_last_error().decode(), (st, lib.ds_last_error())
+
+
+def test_commit_refuses_unaligned_cache(lib):
+    a, keep = _commit_args()
+    bad = (C.c_void_p * 2)(256, 520)
+    a.v_caches = C.cast(bad, C.POINTER(C.c_void_p))
+    assert lib.ds_kv_commit(C.byref(a), None) == B.DS_ERR_INVALID_ARG
+    assert "16-byte aligned" in lib.ds_last_error().decode()
+
+
+def _append_args(**kw):
+    a = B.AppendArgs()
+    B.load().ds_append_args_default(C.byref(a))
+    base = dict(src_k=256, src_v=512, page_table=16, from_lens=32, to_lens=48,
+                batch=1, num_kv_heads=8, head_dim=128, page_size=16, num_pages=10,
+                max_pages=4, capacity=100, out_k=1024, out_v=2048, out_positions=64,
+                out_len=80, workspace=4096, workspace_bytes=256)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status,word", [
+    ("head_dim", 32, B.DS_ERR_UNSUPPORTED, "head_dim"),
+    ("batch", 0, B.DS_ERR_INVALID_ARG, "batch"),
+    ("capacity", -1, B.DS_ERR_INVALID_ARG, "capacity"),
+    ("rope_base", -2.0, B.DS_ERR_INVALID_ARG, "rope_base"),
+    ("rope_base", float("inf"), B.DS_ERR_INVALID_ARG, "rope_base"),
+    ("to_lens", None, B.DS_ERR_INVALID_ARG, "is NULL"),
+    ("out_k", 1032, B.DS_ERR_INVALID_ARG, "aligned"),
+    ("workspace", None, B.DS_ERR_WORKSPACE, "workspace"),
+])
+def test_append_refuses_by_name(lib, field, value, status, word):
+    st = lib.ds_compact_append(C.byref(_append_args(**{field: value})), None)
+    assert st == status and word in lib.ds_last_error().decode(), (st, lib.ds_last_error())
