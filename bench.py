@@ -116,6 +116,15 @@ class ClockSampler:
         return parse_clock_samples(lines, t0, t1)
 
 
+def sampled_launches(steps: int, layers: int, every: int):
+    """(step, layer) pairs whose split pass is bracketed by events: layer l
+    of step s when l = s (mod every), so each layer is sampled in one step of
+    every `every` (all layers when there are fewer than `every`)."""
+    if layers <= every:
+        return [(s, l) for s in range(steps) for l in range(layers)]
+    return [(s, l) for s in range(steps) for l in range(layers) if l % every == s % every]
+
+
 def parse_clock_samples(lines, t0=None, t1=None):
     """Summary of nvidia-smi csv lines (timestamp first) within [t0, t1]
     (host epoch seconds); the nearest sample when none is inside."""
@@ -244,8 +253,8 @@ def _config(wl, st, kv_layout="NHD"):
             "chunk_size": wl.chunk_size, "top_k": wl.top_k,
             "window": wl.window, "vocab": wl.vocab, "accept": wl.accept,
             "rope_base": wl.rope_base, "kv_commit": True,
-            "split_events": f"split pass of layers {EV_EVERY - 1}, "
-                            f"{2 * EV_EVERY - 1}, ... (every {EV_EVERY}th)",
+            "split_events": f"every {EV_EVERY}th layer's split pass, "
+                            "rotating with the step",
             "l2": "inputs larger than L2: every layer has its own "
                   f"{_kv_bytes(wl, st) / 1e6:.0f} MB K/V cache"}
 
@@ -344,15 +353,11 @@ def run_ours(args, wl, rank, world, local_rank):
                       window=wl.window, accept_mode=mode,
                       kv_layout=args.kv_layout, with_commit=True,
                       rope_base=wl.rope_base)
-    # events around the split-pass kernel of every EV_EVERY-th layer
-    # (layers EV_EVERY - 1, 2 EV_EVERY - 1, ...; never layer 0, whose split
-    # follows the step's gather, acceptance and commit rather than another
-    # layer): each event pair sits between two kernels of the step and
-    # costs it a few microseconds, so only a sample of the launches is
-    # bracketed
-    every = min(EV_EVERY, wl.layers)
-    sampled = [(s_, l) for s_ in range(args.steps) for l in range(wl.layers)
-               if l % every == every - 1]
+    # events around a sample of the split-pass launches (each event pair
+    # sits between two kernels of the step and costs it a few
+    # microseconds): every EV_EVERY-th layer, rotating with the step so that
+    # every layer is sampled equally often
+    sampled = sampled_launches(args.steps, wl.layers, EV_EVERY)
     evs = [(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in sampled]
     for e_a, e_b in evs:      # torch creates the CUDA event on first record

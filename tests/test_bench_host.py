@@ -34,3 +34,15 @@ def test_short_region_takes_nearest_sample():
 
 def test_garbage_lines_ignored():
     assert bench.parse_clock_samples(["", "bad line\n"], 0.0, 1.0) is None
+
+
+def test_sampled_launches_cover_every_layer_equally():
+    got = bench.sampled_launches(8, 32, 4)
+    assert len(got) == 8 * 8
+    per_layer = {}
+    for s, l in got:
+        assert l % 4 == s % 4
+        per_layer[l] = per_layer.get(l, 0) + 1
+    assert sorted(per_layer) == list(range(32)) and set(per_layer.values()) == {2}
+    assert bench.sampled_launches(3, 1, 4) == [(0, 0), (1, 0), (2, 0)]
+    assert len(bench.sampled_launches(5, 3, 4)) == 15
