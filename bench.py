@@ -261,7 +261,8 @@ def _config(wl, st, kv_layout="NHD"):
 
 def _traffic_for(src_path: str):
     """DRAM bytes per launch of the split pass from the committed ncu summary,
-    valid only while the kernel source is unchanged since the capture."""
+    valid only while the kernel source (comments aside) is unchanged since
+    the capture."""
     p = os.path.join(ROOT, "profiles", "verify_split_traffic.json")
     if not os.path.exists(p):
         return None
