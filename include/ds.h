@@ -11,7 +11,9 @@
  *   ds_chunk_topk_gather  top-k chunks by salience plus a recent window,
  *                         gathered into a compact contiguous cache;
  *   ds_accept             the accepted path: greedy accept-if-equal or exact
- *                         tree rejection sampling with supplied uniforms;
+ *                         tree rejection sampling with supplied uniforms
+ *                         (ds_accept_static: the same over a scratch the
+ *                         library owns, for callers that cannot allocate);
  *   ds_kv_commit          the accepted path's tree K/V moved behind the root
  *                         in every layer, and the new context lengths;
  *   ds_compact_append     newly committed tokens appended to the compact
