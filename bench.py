@@ -12,8 +12,10 @@ layer (step time / layers; with N replicas, the whole job's step time per
 layer-step: ms / (layers * N)), so lower is better.  Inputs stay resident in
 HBM; every layer's K/V cache is a distinct 537 MB tensor, larger than L2.
 
---impl reference times the float64 CPU oracle on the host cores instead, on
-a bounded sample of the same workload each step.
+--impl reference times the float64 CPU oracle on the host cores instead:
+each step is one whole layer of the same workload (every kv head) plus its
+retrieval and acceptance, and the per-layer figure is extrapolated to the
+workload's layer count with the factor stated in the line.
 """
 from __future__ import annotations
 
@@ -27,6 +29,12 @@ import subprocess
 import sys
 import time
 
+# The oracle's BLAS runs on every host core this process may use: the thread
+# count is fixed before NumPy (or torch) is first imported.
+CORES = len(os.sched_getaffinity(0))
+for _var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ[_var] = str(CORES)
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -36,6 +44,7 @@ UNIT = "us/verify-step/layer"
 DEFAULT_WORKLOAD = "llama8b-128k-32l"
 FALLBACK_HBM_GBS = 6800.0
 EV_EVERY = 4          # split-pass events bracket every 4th layer's launch
+CPU_BASELINE_LAYERS = 4   # whole layers the CPU baseline times
 
 
 def _peaks():
@@ -159,33 +168,33 @@ def parse_clock_samples(lines, t0=None, t1=None):
 # ---------------------------------------------------------------------------
 # oracle timing (CPU baseline and the reference arm)
 
-def oracle_sample(wl, st, layer_inputs, accept_inp, heads_sampled: int):
-    """Times the float64 oracle on a bounded sample of one step: one layer's
-    verify attention restricted to `heads_sampled` kv heads (with their query
-    heads), the top-k gather, and acceptance.  Returns (seconds per full step
-    per layer, description)."""
+def oracle_time(wl, st, layers, src, accept_inp):
+    """Times the float64 oracle on whole layers of one step: verify attention
+    of every kv head for each layer given (all query heads, all nodes, chunk
+    scores summed over those layers), then the top-k gather with the
+    workload's local RoPE over the whole source cache (K and V of every kv
+    head), then acceptance.  Returns a dict of wall-clock seconds."""
     import numpy as np
+    import torch
     from oracle import ref
-    q, k, v = layer_inputs
-    G = wl.num_q_heads // wl.num_kv_heads
-    f64 = lambda t: t.detach().cpu().to(__import__("torch").float64).numpy()
-    qs = f64(q[:, :G * heads_sampled])
-    ks = f64(k[:, :, :heads_sampled])
-    vs = f64(v[:, :, :heads_sampled])
-    t0 = time.perf_counter()
-    _, scores, _ = ref.verify_attention(qs, ks, vs, st.page_table.numpy(),
-                                        st.ctx_lens, st.tree_offsets,
-                                        st.parents, wl.page_size,
-                                        wl.chunk_size)
-    t_verify = (time.perf_counter() - t0) * wl.num_kv_heads / heads_sampled
-    kb = k[:, :, :1].contiguous().view(__import__("torch").int16).numpy() \
-        .view(np.uint16)
-    t0 = time.perf_counter()
+    f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t_layers = []
+    total = 0.0
+    for q, k, v in layers:
+        t0 = time.perf_counter()
+        _, scores, _ = ref.verify_attention(
+            f64(q), f64(k), f64(v), st.page_table.numpy(), st.ctx_lens,
+            st.tree_offsets, st.parents, wl.page_size, wl.chunk_size)
+        total = total + scores
+        t_layers.append(time.perf_counter() - t0)
+    sk, sv = src
     cap = wl.top_k * wl.chunk_size + wl.window
-    ref.gather_compact(kb, kb, st.page_table.numpy(), st.ctx_lens, scores,
-                       wl.page_size, wl.chunk_size, wl.top_k, wl.window, cap)
-    # gather moved one kv head of K twice; scale to all heads of K and V
-    t_gather = (time.perf_counter() - t0) * wl.num_kv_heads
+    t0 = time.perf_counter()
+    ref.gather_compact(bits(sk), bits(sv), st.page_table.numpy(), st.ctx_lens,
+                       total, wl.page_size, wl.chunk_size, wl.top_k, wl.window,
+                       cap, rope_base=wl.rope_base)
+    t_gather = time.perf_counter() - t0
     t0 = time.perf_counter()
     tl = accept_inp.target_logits.cpu().numpy()
     toks = accept_inp.draft_tokens.cpu().numpy()
@@ -196,48 +205,81 @@ def oracle_sample(wl, st, layer_inputs, accept_inp, heads_sampled: int):
     else:
         ref.greedy_accept(tl, toks, st.parents, st.tree_offsets)
     t_accept = time.perf_counter() - t0
-    per_layer = (t_verify * wl.layers + t_gather + t_accept) / wl.layers
-    desc = (f"1 layer of verify attention on {heads_sampled}/{wl.num_kv_heads} "
-            f"kv heads (scaled x{wl.num_kv_heads // heads_sampled}, then x"
-            f"{wl.layers} layers), top-k gather of 1 kv head of K (scaled), "
-            f"full acceptance; divided by {wl.layers} layers")
-    return per_layer, desc
+    return {"layers": t_layers, "gather": t_gather, "accept": t_accept}
 
 
-def cpu_inputs(wl):
-    import torch
+def oracle_summary(wl, t):
+    """Per-layer figure of a whole step from timed layers: the mean timed
+    layer stands for each of the workload's layers (extrapolation factor =
+    layers / timed layers), retrieval and acceptance are timed in full and
+    spread over the layers like the GPU figure."""
+    n = len(t["layers"])
+    per_layer_s = (statistics.mean(t["layers"]) * wl.layers + t["gather"] +
+                   t["accept"]) / wl.layers
+    return {
+        "value_us": per_layer_s * 1e6,
+        "timed_layers": n,
+        "timed_kv_heads": wl.num_kv_heads,
+        "extrapolation_factor": wl.layers / n,
+        "extrapolated": n < wl.layers,
+        "layer_s": [round(x, 3) for x in t["layers"]],
+        "gather_s": round(t["gather"], 3),
+        "accept_s": round(t["accept"], 3),
+        "sample": (f"{n} whole layer(s) of verify attention (all "
+                   f"{wl.num_kv_heads} kv heads, all query heads and nodes) "
+                   f"timed and taken x{wl.layers / n:g} for the step's "
+                   f"{wl.layers} layers; top-k gather with local RoPE and "
+                   f"{wl.accept} acceptance timed in full; divided by "
+                   f"{wl.layers} layers"),
+    }
+
+
+def cpu_inputs(wl, n_layers):
     from long_context_speculative_ds_gb300 import synth
     st = synth.make_structure(wl)
-    q, k, v = synth.make_layer(st, 0, device="cpu")
+    layers = [synth.make_layer(st, l, device="cpu") for l in range(n_layers)]
+    src = synth.make_source_cache(st, device="cpu")
     mode = "reject" if wl.accept == "reject" else "greedy"
     acc = synth.make_accept_inputs(st, mode)
-    return st, (q, k, v), acc
+    return st, layers, src, acc
 
 
 def run_reference(args, wl, rank, world):
+    """The reference arm: the float64 oracle on the host cores.  Each step
+    runs one whole layer (every kv head) plus the retrieval and acceptance;
+    `ms_per_step` is that step's measured wall time, and `value` is the
+    per-layer figure of a whole step with the layer time taken for each of
+    the workload's layers (the fields say by how much)."""
     if rank != 0:
         return
-    cores = len(os.sched_getaffinity(0))
-    st, layer, acc = cpu_inputs(wl)
+    st, layers, src, acc = cpu_inputs(wl, 1)
     for _ in range(args.warmup):
-        oracle_sample(wl, st, layer, acc, 1)
-    per = []
-    desc = ""
+        oracle_time(wl, st, layers, src, acc)
+    runs = []
     for _ in range(args.steps):
-        s, desc = oracle_sample(wl, st, layer, acc, 1)
-        per.append(s)
-    us = statistics.mean(per) * 1e6
+        t0 = time.perf_counter()
+        t = oracle_time(wl, st, layers, src, acc)
+        runs.append((time.perf_counter() - t0, t))
+    step_s = statistics.mean(r[0] for r in runs)
+    merged = {"layers": [x for r in runs for x in r[1]["layers"]],
+              "gather": statistics.mean(r[1]["gather"] for r in runs),
+              "accept": statistics.mean(r[1]["accept"] for r in runs)}
+    summ = oracle_summary(wl, merged)
+    summ["timed_layers"] = 1
+    summ["extrapolation_factor"] = wl.layers
+    summ["layer_s"] = [round(statistics.mean(merged["layers"]), 3)]
+    us = summ.pop("value_us")
     kvb = _kv_bytes(wl, st)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 3),
         "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(us * wl.layers / 1e3, 3),
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": _config(wl, st),
         "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 3),
-        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": cores,
-                         "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": CORES,
+                         "kind": "oracle", **summ},
         "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -552,11 +594,12 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        cst, layer, cacc = cpu_inputs(wl)
-        t, desc = oracle_sample(wl, cst, layer, cacc, 1)
-        line["cpu_baseline"] = {"value": round(t * 1e6, 1), "unit": UNIT,
-                                "cores": len(os.sched_getaffinity(0)),
-                                "kind": "oracle", "sample": desc}
+        n_cpu = min(CPU_BASELINE_LAYERS, wl.layers)
+        cst, clayers, csrc, cacc = cpu_inputs(wl, n_cpu)
+        summ = oracle_summary(wl, oracle_time(wl, cst, clayers, csrc, cacc))
+        us_cpu = summ.pop("value_us")
+        line["cpu_baseline"] = {"value": round(us_cpu, 1), "unit": UNIT,
+                                "cores": CORES, "kind": "oracle", **summ}
     print(json.dumps(line), flush=True)
 
 

@@ -431,7 +431,8 @@ def rejection_accept(target_logits, draft_logits, draft_tokens, parents,
 
     `mutation` plants one of the known bugs (test-only): skip_accept,
     resample_from_p, unnormalised_residual, wrong_uniform.  `record`, if a
-    list, receives one dict per decision with its margin |u - ratio|.
+    list, receives one dict per decision with its margin |u - ratio| (the
+    bonus draw's also carries u and the normalised CDF it was drawn from).
     """
     assert mutation is None or mutation in MUTATIONS
     target_logits = np.asarray(target_logits, dtype=np.float64)
@@ -476,7 +477,7 @@ def rejection_accept(target_logits, draft_logits, draft_tokens, parents,
             c = np.cumsum(p)
             S = c[-1]
             lo = c[x - 1] / S if x > 0 else 0.0
-            record.append(dict(seq=b, kind="bonus", node=i,
+            record.append(dict(seq=b, kind="bonus", node=i, u=u1, cdf=c / S,
                                margin=min(abs(u1 - lo), abs(u1 - c[x] / S))))
         paths.append(path)
         n_acc.append(len(path))

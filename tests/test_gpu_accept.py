@@ -2,8 +2,9 @@
 
 Greedy: accepted paths, counts and bonus tokens bit-exact against the oracle.
 Rejection: the same, except where the oracle's own decision margin
-|u - p/q| (or, for the bonus draw, |u - CDF_x/S|) is below 1e-6; once a
-sequence passes such a decision the rest of its walk is unconstrained.
+|u - p/q| (or, for the bonus draw, |u - CDF_x/S|) is below 1e-6: such a
+sequence is compared up to that decision only, and each test allows at most
+one such sequence.
 """
 import numpy as np
 import pytest
@@ -28,6 +29,7 @@ def _run_accept(step):
 
 
 def _check(st, inp, step, mode):
+    """Returns (oracle paths, sequences exempted by a near-tie decision)."""
     g_paths, g_n, g_bonus, raw = _run_accept(step)
     for b in range(len(g_n)):
         assert (raw[b, g_n[b]:] == -1).all()
@@ -36,17 +38,13 @@ def _check(st, inp, step, mode):
     if mode == "greedy":
         paths, n, bonus = ref.greedy_accept(tl, toks, st.parents, st.tree_offsets)
         assert g_paths == paths and g_n == n and g_bonus == bonus
-        return paths
+        return paths, 0
     rec = []
     paths, n, bonus = ref.rejection_accept(
         tl, inp.draft_logits.cpu().numpy(), toks, st.parents, st.tree_offsets,
         inp.uniforms.cpu().numpy(), record=rec)
-    exempt = {r["seq"] for r in rec if r["margin"] < H.EXEMPT}
-    for b in range(len(g_n)):
-        if b in exempt:
-            continue
-        assert g_paths[b] == paths[b] and g_bonus[b] == bonus[b], b
-    return paths
+    exempt = H.check_rejection(g_paths, g_bonus, paths, bonus, rec, "rejection")
+    return paths, exempt
 
 
 @pytest.mark.parametrize("mode", ["greedy", "reject"])
@@ -54,7 +52,7 @@ def test_tiny_workload(mode):
     wl = synth.WORKLOADS["tiny"]
     st, inp, _ = H.build_case(wl, mode=mode)
     step = H.make_step(wl, inp, mode)
-    _check(st, inp, step, mode)
+    assert _check(st, inp, step, mode)[1] <= 1
 
 
 @pytest.mark.parametrize("mode", ["greedy", "reject"])
@@ -63,7 +61,7 @@ def test_many_random_trees(mode, vocab):
     """Batches of random trees (up to 64 nodes, duplicates among siblings
     allowed), vocabularies that are and are not multiples of 4."""
     wl = synth.tiny_workload(batch=12, vocab=vocab, max_depth=10, max_branch=4)
-    accepted = 0
+    accepted = exempt = 0
     for seed in range(4):
         rng = np.random.default_rng(seed)
         trees = [int(x) for x in rng.integers(1, 65, size=12)]
@@ -72,9 +70,11 @@ def test_many_random_trees(mode, vocab):
                                   ctx_lens=[32] * 12, tree_sizes=trees,
                                   draft="noisy")
         step = H.make_step(wl, inp, mode)
-        paths = _check(st, inp, step, mode)
+        paths, ex = _check(st, inp, step, mode)
         accepted += sum(len(p) for p in paths)
+        exempt += ex
     assert accepted > 0    # the accept branch is exercised
+    assert exempt <= 1
 
 
 def test_one_hot_target_rejection_equals_greedy():
@@ -113,4 +113,4 @@ def test_full_size(name, mode):
     wl = synth.WORKLOADS[name]
     st, inp, _ = H.build_case(wl, layers=1, mode=mode)
     step = H.make_step(wl, inp, mode)
-    _check(st, inp, step, mode)
+    assert _check(st, inp, step, mode)[1] <= 1

@@ -20,21 +20,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _check_gather(wl, st, inp, step, scores_np, layout):
-    cap = step.capacity
-    exp = ref.gather_compact(H.bits(inp.src_k), H.bits(inp.src_v),
-                             st.page_table.numpy(), st.ctx_lens, scores_np,
-                             wl.page_size, wl.chunk_size, wl.top_k, wl.window,
-                             cap, layout=layout)
-    ids = step.out_chunk_ids.cpu().numpy()[:, :wl.top_k]
-    np.testing.assert_array_equal(ids, exp["chunk_ids"])
-    np.testing.assert_array_equal(step.out_len.cpu().numpy(), exp["out_len"])
-    np.testing.assert_array_equal(step.out_positions.cpu().numpy(),
-                                  exp["positions"])
-    ok, ov = H.bits(step.out_k), H.bits(step.out_v)
-    for b in range(wl.batch):
-        n = exp["out_len"][b]
-        np.testing.assert_array_equal(ok[b, :n], exp["out_k"][b, :n])
-        np.testing.assert_array_equal(ov[b, :n], exp["out_v"][b, :n])
+    H.check_gather(wl, st, inp, step, scores_np, layout)
 
 
 def _set_scores(step, scores_np):
@@ -103,16 +89,7 @@ def test_full_size_from_verify_scores(name):
     gs = step.scores.double().cpu().numpy()
     _check_gather(wl, st, inp, step, gs, "NHD")
     _, rs, _ = H.oracle_layer(wl, st, inp, 0, "NHD", step.max_chunks)
-    for b in range(wl.batch):
-        L = st.ctx_lens[b]
-        got = ref.select_chunks(gs[b], L, wl.chunk_size, wl.top_k, wl.window)
-        want = ref.select_chunks(rs[b], L, wl.chunk_size, wl.top_k, wl.window)
-        if got != want:
-            n = ref.candidate_count(L, wl.chunk_size, wl.window)
-            srt = np.sort(rs[b, :n])[::-1]
-            sk, sk1 = srt[wl.top_k - 1], srt[wl.top_k]
-            assert abs(sk - sk1) <= 1e-3 * sk, "selection differs beyond a near-tie"
-        assert set(st.planted_chunks[b]) <= set(got), "a planted chunk was missed"
+    H.check_selection_vs_f64(wl, st, gs, rs)
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])

@@ -4,8 +4,9 @@ Bars: attention output |gpu - ref| <= 2e-3 + 1e-2 |ref| elementwise; chunk
 scores within 1e-3 relative.  Small cases span several key tiles, ragged
 tails, empty contexts, single nodes, chains, all supported head dims, page
 sizes, chunk sizes, group sizes (including two row groups) and both cache
-layouts; the five workloads run at full size for one layer (two for the
-layer-summed scores).
+layouts; the four large workloads run at full size for one layer here, and
+the headline and ragged workloads run as whole multi-layer steps (summed
+scores, retrieval, acceptance) in test_gpu_fullstep.py.
 """
 import math
 

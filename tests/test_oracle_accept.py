@@ -193,7 +193,7 @@ def test_g1_emitted_tokens_follow_exact_ar_marginal():
     tv, pval = _tv_and_p(counts, model.exact_joint())
     floor = math.sqrt(V_SMALL * V_SMALL / (2 * math.pi * counts.sum()))
     assert tv < 0.02, (tv, floor)
-    assert pval > 1e-3, pval
+    assert pval > 0.01, pval
 
 
 @pytest.mark.parametrize("mutation", ref.MUTATIONS)
@@ -201,7 +201,7 @@ def test_g1_catches_each_planted_bug(mutation):
     model = TinyModel(3)
     counts = _emit_pairs(model, 20000, seed=2, mutation=mutation)
     tv, pval = _tv_and_p(counts, model.exact_joint())
-    # the gate of the correct walk is (tv < 0.02 and pval > 1e-3); each bug
+    # the gate of the correct walk is (tv < 0.02 and pval > 0.01); each bug
     # must fail it decisively
     assert tv >= 0.02 or pval < 1e-6, (mutation, tv, pval)
     assert pval < 1e-6, (mutation, tv, pval)

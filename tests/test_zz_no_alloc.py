@@ -77,19 +77,16 @@ def test_static_scratch_matches_workspace_entry(mode):
     path, n, bonus = want
     tl = inp.target_logits.cpu().numpy()
     toks = inp.draft_tokens.cpu().numpy()
+    g_paths = [list(path[b, :n[b]]) for b in range(len(n))]
     if mode == "greedy":
         rp, rn, rb = ref.greedy_accept(tl, toks, st.parents, st.tree_offsets)
-        exempt = set()
+        assert g_paths == rp and list(bonus) == rb
     else:
         rec = []
         rp, rn, rb = ref.rejection_accept(
             tl, inp.draft_logits.cpu().numpy(), toks, st.parents, st.tree_offsets,
             inp.uniforms.cpu().numpy(), record=rec)
-        exempt = {r["seq"] for r in rec if r["margin"] < H.EXEMPT}
-    for b in range(len(rn)):
-        if b in exempt:
-            continue
-        assert list(path[b, :n[b]]) == rp[b] and bonus[b] == rb[b], b
+        assert H.check_rejection(g_paths, list(bonus), rp, rb, rec, "static") <= 1
 
 
 @pytest.mark.gpu
