@@ -301,17 +301,21 @@ ds_status ds_accept(const ds_accept_args* args, void* stream);
  *
  * Same arguments, kernels and results as ds_accept, except that
  * args->workspace must be NULL and args->workspace_bytes 0: the scratch
- * (a status word and one 48-byte record per tree node) is a fixed array in
+ * (a status word and one 112-byte record per tree node) is a fixed array in
  * device global memory inside the library, DS_ACCEPT_STATIC_MAX_NODES
- * records long (about 193 KiB per device).  Nothing is allocated, on the
+ * records long (about 448 KiB per device).  Nothing is allocated, on the
  * device or through any library, by this call.
  *
  * Refused with DS_ERR_UNSUPPORTED: args->n_nodes > DS_ACCEPT_STATIC_MAX_NODES
  * (use ds_accept).  Refused with DS_ERR_INVALID_ARG: a non-NULL workspace.
  *
  * Setup: the first call made while a given device is current looks up the
- * array's address on that device (cudaGetSymbolAddress); make that first
- * call before capturing `stream` into a graph.  Each call then enqueues, on
+ * array's address on that device (cudaGetSymbolAddress) and keeps it for
+ * the life of the process; make that first call before capturing `stream`
+ * into a graph.  The kept address belongs to the device's context of that
+ * time: after cudaDeviceReset (or any teardown of the primary context) the
+ * array is reloaded elsewhere, so do not call ds_accept_static again in
+ * that process.  Each call then enqueues, on
  * `stream`, a zeroing of the status word (the one part of the scratch that
  * must start at zero; the node records are written before they are read)
  * and the acceptance kernels.

@@ -38,13 +38,31 @@ struct AcceptLayout {
   size_t total;
 };
 
-// Per-node statistics written by the acceptance node pass.
+// Slices of the vocabulary into which the greedy argmax pass cuts a node's
+// target row (one CTA each).
+constexpr int kArgmaxSlices = 8;
+
+// Slices of the greedy argmax pass for a vocabulary: about 4096 logits or more
+// per CTA, at most kArgmaxSlices.
+inline int accept_argmax_slices(int vocab) {
+  const int s = (vocab + 4095) / 4096;
+  return s < 1 ? 1 : (s > kArgmaxSlices ? kArgmaxSlices : s);
+}
+
+// Per-node statistics written by the acceptance node passes.  The rejection
+// fields are the fp32 scalars the node pass itself used, so that the walk
+// evaluates p(x), q(x) and the residual chain at a token with exactly the
+// node pass's float operations.
 struct NodeStats {
-  double m_t, s_t;      // target: max logit, sum exp(l - m)
-  double m_d, s_d;      // draft:  max logit, sum exp(l - m)
-  double z_after;       // residual normaliser after rejecting this node (as a child)
-  int32_t argmax_t;     // lowest index of the target maximum
-  int32_t bonus_stop;   // bonus token if the walk stops at this node (rejection)
+  float m_t, inv_s_t;   // target: max logit, 1 / sum exp(l - max)   (rejection)
+  float m_d, inv_s_d;   // draft:  the same                          (rejection)
+  float zinv_after;     // 1 / Z of the residual step that rejecting this
+                        // node (as a child) makes; 0 when Z = 0     (rejection)
+  int32_t bonus_stop;   // bonus token if the walk stops here        (rejection)
+  uint64_t amax[kArgmaxSlices];   // greedy: per slice, the largest key
+                                  // (order-preserving bits of the logit << 32
+                                  // | ~index), so the maximum key is the
+                                  // largest logit at its lowest index
 };
 
 VerifyLayout verify_layout(const ds_verify_args& a, int num_sms);
