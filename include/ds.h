@@ -90,9 +90,11 @@ int32_t ds_abi_version(void);
  * their own struct layouts before the first call. */
 int64_t ds_struct_size(int32_t which);
 
-/* Zero the workspace's status word (bytes 0..255 of any workspace).  Call
- * once after allocating a workspace and whenever the sticky bits should be
- * cleared.  Enqueued on `stream`. */
+/* Zero the whole workspace: the status word (bytes 0..255 of any workspace)
+ * and the verify call's split counters behind it (which every completed
+ * call leaves at zero).  Call once after allocating a workspace, whenever the
+ * sticky bits should be cleared, and after a call that set DS_DEV_TIMEOUT (an
+ * aborted call can leave counters behind).  Enqueued on `stream`. */
 ds_status ds_workspace_init(void* workspace, size_t workspace_bytes,
                             void* stream);
 
@@ -177,7 +179,7 @@ ds_status ds_verify_attn_workspace_size(const ds_verify_args* args,
 
 /* Enqueue the verify step.  Output `out` and `chunk_scores` are complete
  * when the work on `stream` completes.  The workspace must not be shared by
- * calls that may overlap on the GPU.  Its three kernels are launched as
+ * calls that may overlap on the GPU.  Its two kernels are launched as
  * programmatic dependents of the preceding work on `stream` (each waits for
  * that work to complete before it reads or writes memory, so ordering is
  * that of the stream; only launch latency overlaps); an event recorded

@@ -106,6 +106,8 @@ VerifyLayout verify_layout(const ds_verify_args& a, int num_sms) {
   L.target_ctas = num_sms;
   L.max_items = num_sms + a.batch * a.num_kv_heads * L.rg_max;
   size_t off = kStatusBytes;
+  L.counters = off;
+  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * sizeof(uint32_t));
   L.o_part = off;
   off = align_up(off + (size_t)L.max_items * kRowsPerItem * a.head_dim * sizeof(float));
   L.lse_part = off;
@@ -155,7 +157,7 @@ ds_status ds_workspace_init(void* workspace, size_t workspace_bytes, void* strea
   REQUIRE(workspace_bytes >= ds::kStatusBytes, DS_ERR_WORKSPACE,
           "workspace_bytes %zu below the %zu-byte status region", workspace_bytes,
           ds::kStatusBytes);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, ds::kStatusBytes,
+  cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes,
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ds_workspace_init");
   return ok();

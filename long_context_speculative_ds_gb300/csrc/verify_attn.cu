@@ -1,18 +1,22 @@
 // Tree-verify attention over a paged bf16 KV cache with fused chunk salience.
 //
-// Three launches per call:
+// Two launches per call:
 //   1. split pass   (tcgen05 kernel in verify_tc.cu) one CTA per work item
 //                   (sequence, kv head, row group, split of key tiles):
 //                   online softmax over its key tiles, writing
 //                   the split's normalised output, its row log2-sum-exp, and
 //                   for every context chunk in its range the chunk's log2
-//                   attention mass per row (log2 sum_{t in chunk} 2^{s_t}).
-//   2. combine      log-sum-exp merge of the splits of each row -> out, and the
-//                   final row log2-sum-exp.
-//   3. finalize     chunk score = sum over rows of 2^{chunk mass - row lse},
-//                   the mass under the full softmax denominator, summed over
-//                   all query heads and nodes (vllm-diffspec README,
-//                   "Architecture": chunks scored from paged target KV).
+//                   attention mass per row (log2 sum_{t in chunk} 2^{s_t});
+//                   the last split of each row group to finish also forms
+//                   the rows' final log2-sum-exp.
+//   2. finish       in one grid, independently:
+//                   combine: log-sum-exp merge of the splits of each row ->
+//                   out;
+//                   finalize: chunk score = sum over rows of 2^{chunk mass -
+//                   row lse}, the mass under the full softmax denominator,
+//                   summed over all query heads and nodes (vllm-diffspec
+//                   README, "Architecture": chunks scored from paged target
+//                   KV).
 // Scores are carried in log2 units (s * scale * log2 e) throughout.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -27,22 +31,32 @@
 namespace ds {
 
 // ---------------------------------------------------------------------------
-// combine: one warp per (sequence, kv head, row group, row).  Both round
-// trips of a row are issued together: the outputs of its first kCombBatch
-// splits (lane-parallel over columns) and the split log2-sum-exps
-// (lane-parallel over splits); the weights 2^{lse_s - lse} are then
-// broadcast from the lane that holds split s.
+// finish: one launch, two independent jobs, both reading the split pass's
+// outputs and the final row log2-sum-exp that the last split of each row
+// group formed.
+//
+// combine (the first n_comb CTAs): one warp per (sequence, kv head, row
+//   group, row).  The outputs of the row's first kCombBatch splits
+//   (lane-parallel over columns), the split log2-sum-exps (lane-parallel
+//   over splits) and the row's final log2-sum-exp are loaded in one round
+//   trip; the weights 2^{lse_s - lse} are broadcast from the lane that holds
+//   split s.
+// finalize (the rest): one warp per (chunk, sequence).  Lane i covers rows
+//   4i .. 4i + 3 and 128 + 4i .. 128 + 4i + 3 of every (kv head, row group)
+//   with 16-byte loads; four (kv head, row group) combinations per round.
 constexpr int kCombBatch = 24;
+constexpr int kFinishThreads = 256;
+constexpr int kFinishWarps = kFinishThreads / 32;
 
 template <int D>
-__global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
+DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   __shared__ Plan s_plan;
-  grid_dep_wait();
-  grid_dep_launch_dependents();
+  const int row_blocks = kRowsPerGroup / kFinishWarps;
+  const int grp = blk / row_blocks, rblk = blk % row_blocks;
   const int per_b = a.plan.num_kv_heads * a.plan.rg_max;
-  const int b = blockIdx.x / per_b;
-  const int h = (blockIdx.x / a.plan.rg_max) % a.plan.num_kv_heads;
-  const int rgi = blockIdx.x % a.plan.rg_max;
+  const int b = grp / per_b;
+  const int h = (grp / a.plan.rg_max) % a.plan.num_kv_heads;
+  const int rgi = grp % a.plan.rg_max;
   if (threadIdx.x < 32) {
     Plan p = plan_find(a.plan, b, 0);
     if (threadIdx.x == 0) s_plan = p;
@@ -52,7 +66,7 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
   const SeqPlan& sq = p.seq;
   if (p.b < 0 || rgi >= sq.rg) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * 8 + warp;
+  const int r = rblk * kFinishWarps + warp;
   const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
   if (r >= rows_here) return;
   const int G = a.plan.group;
@@ -82,14 +96,8 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
     if (k < ns) load_o(k, x[k]);
   }
   const float l0 = lane < ns ? __ldg(lp + (int64_t)lane * kRowsPerGroup) : -CUDART_INF_F;
-  float mx = l0;
-  for (int s = lane + 32; s < ns; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * kRowsPerGroup));
-  mx = warp_max(mx);
-  float sum = lane < ns ? exp2f(l0 - mx) : 0.f;
-  for (int s = lane + 32; s < ns; s += 32) sum += exp2f(__ldg(lp + (int64_t)s * kRowsPerGroup) - mx);
-  sum = warp_sum(sum);
-  const float lse = mx + log2f(sum);
-
+  const float lse = __ldg(a.row_lse + ((((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max +
+                                        rgi) * kRowsPerGroup + r));
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
@@ -133,23 +141,13 @@ __global__ void __launch_bounds__(256) verify_combine(VerifyKArgs a) {
     for (int e = 0; e < E; e += 2)
       *reinterpret_cast<__nv_bfloat162*>(out + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
   }
-  if (lane == 0)
-    a.row_lse[(((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi) * kRowsPerGroup + r] = lse;
 }
 
-// ---------------------------------------------------------------------------
-// finalize: one warp per (chunk, sequence), four chunks per CTA.  Lane i
-// covers rows 4i .. 4i + 3 and 128 + 4i .. 128 + 4i + 3 of every (kv head,
-// row group) with 16-byte loads; four (kv head, row group) combinations are
-// loaded per round, 16 loads in flight per lane.
-constexpr int kFinWarps = 4;
-
-__global__ void __launch_bounds__(32 * kFinWarps) chunk_finalize(VerifyKArgs a) {
-  grid_dep_wait();
-  grid_dep_launch_dependents();
-  const int b = blockIdx.y;
+DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
+  const int nblk_b = (a.plan.max_chunks + kFinishWarps - 1) / kFinishWarps;
+  const int b = blk / nblk_b;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * kFinWarps + warp;
+  const int c = (blk % nblk_b) * kFinishWarps + warp;
   const SeqPlan sq = seq_sizes(a.plan, b, false);
   const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
   if (c >= n_ch) return;
@@ -198,6 +196,14 @@ __global__ void __launch_bounds__(32 * kFinWarps) chunk_finalize(VerifyKArgs a) 
   }
 }
 
+template <int D>
+__global__ void __launch_bounds__(kFinishThreads) verify_finish(VerifyKArgs a, int n_comb) {
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if ((int)blockIdx.x < n_comb) combine_row<D>(a, blockIdx.x);
+  else finalize_chunk(a, blockIdx.x - n_comb);
+}
+
 // ---------------------------------------------------------------------------
 
 cudaError_t launch_split_tc(const VerifyKArgs& k, const ds_verify_args& a,
@@ -211,14 +217,12 @@ static cudaError_t launch_d(const VerifyKArgs& k, const ds_verify_args& a,
   cudaError_t e = launch_split_tc(k, a, L, stream);
   if (e != cudaSuccess) return e;
   if (ev1) cudaEventRecord(ev1, stream);
-  dim3 gc(batch * k.plan.num_kv_heads * L.rg_max, kRowsPerGroup / 8);
-  e = launch_dependent(verify_combine<D>, gc, dim3(256), 0, stream, k);
-  if (e != cudaSuccess) return e;
-  if (k.plan.max_chunks > 0) {
-    dim3 gf((k.plan.max_chunks + kFinWarps - 1) / kFinWarps, batch);
-    e = launch_dependent(chunk_finalize, gf, dim3(32 * kFinWarps), 0, stream, k);
-  }
-  return e;
+  const int n_comb = batch * k.plan.num_kv_heads * L.rg_max * (kRowsPerGroup / kFinishWarps);
+  const int n_fin = k.plan.max_chunks > 0
+                        ? batch * ((k.plan.max_chunks + kFinishWarps - 1) / kFinishWarps)
+                        : 0;
+  return launch_dependent(verify_finish<D>, dim3(n_comb + n_fin), dim3(kFinishThreads), 0,
+                          stream, k, n_comb);
 }
 
 cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
@@ -253,6 +257,7 @@ cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
   }
   const float scale = a.scale != 0.f ? a.scale : 1.0f / sqrtf((float)a.head_dim);
   k.scale_log2 = scale * kLog2e;
+  k.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   k.o_part = reinterpret_cast<float*>(ws + L.o_part);
   k.lse_part = reinterpret_cast<float*>(ws + L.lse_part);
   k.clse = reinterpret_cast<float*>(ws + L.clse);

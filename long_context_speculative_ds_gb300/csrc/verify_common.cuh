@@ -18,6 +18,7 @@ struct VerifyKArgs {
   int32_t num_q_heads, num_pages;
   int64_t page_stride, tok_stride, head_stride;   // elements
   float scale_log2;
+  uint32_t* counters;
   float* o_part;
   float* lse_part;
   float* clse;

@@ -88,6 +88,7 @@ struct Ctrl {
   int32_t parents[DS_MAX_TREE_NODES];
   uint64_t anc[DS_MAX_TREE_NODES];
   uint32_t where[5];   // last wait site of loader, issuer 0, softmax 0, softmax 1, issuer 1
+  int last;            // this CTA is the last split of its row group to finish
 };
 
 template <int D>
@@ -459,6 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npg = kTileKeys / P;
       const int nops = npg;                       // TMA boxes (one per page) per tile
       const int32_t* ptab = a.page_table + (int64_t)p.b * a.plan.max_pages;
+      // K and V are read once: evict-first, so that the stream leaves the
+      // split outputs and chunk masses the finish kernel reads in L2
+      const uint64_t kv_policy = l2_evict_first();
       if (lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -523,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = dst + lane * P * D * 2;
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
           if (hnd)
-            tma_load_5d(d, m, full, 0, 0, 0, 0, pg * a.plan.num_kv_heads + kvh);
+            tma_load_5d_hint(d, m, full, 0, 0, 0, 0, pg * a.plan.num_kv_heads + kvh, kv_policy);
           else
-            tma_load_5d(d, m, full, 0, 0, kvh * NH, 0, pg);
+            tma_load_5d_hint(d, m, full, 0, 0, kvh * NH, 0, pg, kv_policy);
         }
         if (partial) {
           // the one page with ps < valid_end < ps + P: plain 16-byte loads,
@@ -814,6 +818,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     flag(a.plan.status, DS_DEV_TIMEOUT);
     if (diag[1] == blockIdx.x)
       for (int i = 0; i < 5; ++i) diag[2 + i] = ctrl->where[i];
+  }
+  // The last split of a (sequence, kv head, row group) to finish forms the
+  // rows' final log2-sum-exp from every split's, so that the finish kernel
+  // can merge outputs and normalise chunk masses independently.  Every split
+  // counts (a timed-out one too), and the last resets the counter to zero
+  // for the next call.
+  if (active && nt > 0) {
+    const int64_t cidx = ((int64_t)p.b * a.plan.num_kv_heads + kvh) * a.plan.rg_max + rgi;
+    if (threadIdx.x == 0) {
+      __threadfence();            // this split's outputs before its arrival
+      const uint32_t prev = atomicAdd(a.counters + cidx, 1u);
+      const int last = prev + 1 == (uint32_t)sq.splits;
+      if (last) {
+        a.counters[cidx] = 0u;
+        __threadfence();          // the other splits' outputs before reading them
+      }
+      ctrl->last = last;
+    }
+    __syncthreads();
+    if (ctrl->last) {
+      const int64_t base = (int64_t)sq.item_base + (kvh * sq.rg + rgi) * sq.splits;
+      for (int r = threadIdx.x; r < rows_here; r += kThreads) {
+        const float* lp = a.lse_part + base * kRowsPerGroup + r;
+        float mx = -CUDART_INF_F;
+        for (int sp = 0; sp < sq.splits; ++sp)
+          mx = fmaxf(mx, __ldcg(lp + (int64_t)sp * kRowsPerGroup));
+        float sum = 0.f;
+        if (mx != -CUDART_INF_F)
+          for (int sp = 0; sp < sq.splits; ++sp)
+            sum += exp2f(__ldcg(lp + (int64_t)sp * kRowsPerGroup) - mx);
+        a.row_lse[cidx * kRowsPerGroup + r] =
+            sum > 0.f ? mx + log2f(sum) : -CUDART_INF_F;
+      }
+    }
   }
   if (warp == 1) {
     if (active && nt > 0 && lane == 0) {

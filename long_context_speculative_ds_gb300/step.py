@@ -147,11 +147,9 @@ class VerifyStep:
             self.commit(stream)
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one step: 3 per layer (split pass, combine,
-        chunk finalize), 2 for top-k + gather, 2 for acceptance, 1 for the
-        commit."""
-        fin = 1 if self.max_chunks > 0 else 0
-        return self.layers * (2 + fin) + 2 + 2 + (1 if self.with_commit else 0)
+        """Kernel launches of one step: 2 per layer (split pass, finish),
+        2 for top-k + gather, 2 for acceptance, 1 for the commit."""
+        return self.layers * 2 + 2 + 2 + (1 if self.with_commit else 0)
 
     def device_status(self) -> int:
         s = 0
