@@ -103,6 +103,8 @@ struct Cfg {
   // Q (2 tiles) + K ring (2 slots) + V ring (3 slots) + control block
   static constexpr size_t smem = 7 * TB + sizeof(Ctrl) + 1024;
   static_assert(smem <= 232448, "dynamic shared memory above the 227 KB a block can have");
+  // the epilogue stages four warps' 32 x 32-float tiles inside one Q tile
+  static_assert(4 * 32 * 32 * 4 <= TB, "output staging must fit in a Q tile");
 };
 
 // One 64-key unit of one softmax thread (one query row): loads the row's 64
@@ -234,14 +236,27 @@ DS_DEV void softmax_unit(const uint32_t tS, const uint32_t tP, const uint32_t vw
 
 // Output of one softmax thread after its last tile: O / l (merged with the
 // other group's partial result in key mode) and the row's log2-sum-exp.
+// The rows are written through a per-warp staging tile in shared memory
+// (`stage`, 32 rows x 32 floats = 4 KB, idle by then; 16-byte chunk c of row
+// r stored at chunk c ^ (r % 8), so that eight consecutive lanes touch all
+// 32 banks both when a thread writes its row and when a lane reads a row
+// segment): each thread writes its row's 32-column slice, then each warp
+// store writes four rows' 128-byte segments, so the global writes are whole
+// segments instead of 32 rows' scattered 16 bytes.
+constexpr int kStageStride = 32;   // floats per staged row
+
 template <int D>
 __device__ __noinline__ void write_row_output(const bool row_mode, const int g, const bool ok,
                                               const int nt1, const uint32_t tO, const int lrow,
-                                              const bool row_ok, const float m2, const float l,
-                                              float* __restrict__ merge_buf, float* m1buf,
-                                              float* l1buf, float* __restrict__ op,
+                                              const int rows_left, const float m2,
+                                              const float l, float* __restrict__ merge_buf,
+                                              float* m1buf, float* l1buf,
+                                              float* __restrict__ stage,
+                                              float* __restrict__ op_warp,
                                               float* __restrict__ lse_out) {
   using namespace ptx;
+  const int lane = threadIdx.x & 31;
+  const bool row_ok = (lrow & 31) < rows_left;
   if (!row_mode && g == 1) {
     if (ok && nt1 > 0) {
 #pragma unroll 1
@@ -281,19 +296,31 @@ __device__ __noinline__ void write_row_output(const bool row_mode, const int g, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) r[i] = 0u;
     }
-    if (row_ok) {
+    // this thread's row: 32 columns into the staging tile
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float v[4];
+    for (int i = 0; i < 32; i += 4) {
+      float v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float o = __uint_as_float(r[i + e]) * sc0;
-          if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
-          v[e] = o * inv;
-        }
-        *reinterpret_cast<float4*>(op + c4 * 32 + i) = make_float4(v[0], v[1], v[2], v[3]);
+      for (int e = 0; e < 4; ++e) {
+        float o = __uint_as_float(r[i + e]) * sc0;
+        if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
+        v[e] = o * inv;
+      }
+      *reinterpret_cast<float4*>(stage + lane * kStageStride + 4 * ((i >> 2) ^ (lane & 7))) =
+          make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncwarp();
+    // rows 4k + lane / 8, columns 4 (lane % 8) .. + 3 of the slice
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int rr = 4 * k + (lane >> 3), cc = 4 * (lane & 7);
+      if (rr < rows_left) {
+        const float4 v = *reinterpret_cast<const float4*>(
+            stage + rr * kStageStride + 4 * ((lane & 7) ^ (rr & 7)));
+        *reinterpret_cast<float4*>(op_warp + (int64_t)rr * D + c4 * 32 + cc) = v;
       }
     }
+    __syncwarp();
   }
   if (row_ok) *lse_out = lt > 0.f ? mt + __log2f(lt) : -CUDART_INF_F;
 }
@@ -307,8 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using namespace ptx;
   constexpr int TB = Cfg<D>::TB;
   constexpr int NH = Cfg<D>::NH;
-  grid_dep_wait();
-  grid_dep_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -330,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_addr(&ctrl->bar[i]); };
 
   // ---------------------------------------------------------------- set-up
-  if (warp == 0) {
-    Plan p = plan_find(a.plan, -1, blockIdx.x);
-    if (lane == 0) ctrl->plan = p;
-  } else if (warp == 1 && lane == 0) {
+  // Barriers and tensor memory touch no global memory, so they are set up
+  // before waiting for the preceding kernel of the stream; everything that
+  // reads the call's inputs comes after the wait.
+  if (warp == 1 && lane == 0) {
     mbar_init(bar(kQFull), 1);
     for (int s = 0; s < 6; ++s) {
       mbar_init(bar(kKFull + s), 1);
@@ -355,6 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
     tmem_relinquish();
+  }
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (warp == 0) {
+    Plan p = plan_find(a.plan, -1, blockIdx.x);
+    if (lane == 0) ctrl->plan = p;
   }
   tc_fence_before();
   __syncthreads();
@@ -804,9 +835,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       else __syncwarp();
       if (ok) tc_fence_after();
       const int nt1 = row_mode ? 0 : ntiles(1);    // tiles of group 1 in key mode
-      write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, row_ok, m2, l, merge_buf, m1buf,
-                          l1buf,
-                          a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + grow_local) * D,
+      // staging (4 warps x 4 KB, within a Q tile even at head_dim 64): the
+      // group's own Q tile, idle once its MMAs are complete (key mode: Q
+      // tile 0, idle once both groups' are)
+      float* stage = reinterpret_cast<float*>(smem + (row_mode ? g * TB : 0)) +
+                     q4 * 32 * kStageStride;
+      const int warp_row0 = grow_local - lane;       // first row of this warp
+      write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, rows_here - warp_row0, m2, l,
+                          merge_buf, m1buf, l1buf, stage,
+                          a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + warp_row0) * D,
                           a.lse_part + (int64_t)blockIdx.x * kRowsPerGroup + grow_local);
     }
   }
