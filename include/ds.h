@@ -210,9 +210,10 @@ ds_status ds_verify_attn(const ds_verify_args* args, void* stream);
  *   dual-view draft cache, canonical pre-RoPE KV at absolute positions and a
  *   compact cache with local draft RoPE positions): row i of out_k is the
  *   source row rotated to position i, pair (j, j + D/2) by the angle
- *   i * rope_base^(-2j/D), j < D/2, rounded to bf16.  The angle is formed
- *   and reduced modulo 2 pi in float64 and rotated in float32, so a value
- *   can differ from the exactly rounded result by one bf16 unit.  V is
+ *   i * rope_base^(-2j/D), j < D/2, rounded to bf16.  The angle is reduced
+ *   modulo one turn exactly (64-bit fixed point), its sine and cosine taken
+ *   in float32 and the pair rotated in float32, so a value can differ from
+ *   the exactly rounded result by one bf16 unit.  V is
  *   always copied byte for byte; rope_base = 0 copies K byte for byte too.
  *
  * Constraints: chunk_size a multiple of page_size; head_dim 64 or 128;

@@ -37,7 +37,9 @@ struct GatherKArgs {
   int32_t* out_chunk_ids;
   uint32_t* status;
   float rope_base;           // > 0: rotate K to its local position
-  double inv_freq[64];       // rope_base^(-2j/D), j < D/2 (host-computed)
+  // frequency j of the rotation as a 64-bit fraction of a turn:
+  // round(rope_base^(-2j/D) / (2 pi) * 2^64), j < D/2 (host-computed)
+  unsigned long long rope_turn[64];
   const int32_t* from_lens;  // compact append: tokens [from, to) of each sequence
   const int32_t* to_lens;
 };
@@ -77,6 +79,20 @@ DS_DEV int block_excl_scan(int v, int* s_warp, int* total) {
   *total = s_warp[32];
   __syncthreads();
   return r;
+}
+
+// Frequencies of the local RoPE as 64-bit fractions of a turn: the exact
+// value of 2^64 * base^(-2j/D) / (2 pi), rounded once (double has 53 bits;
+// the product's error stays below 2^-37 of a turn at every position below
+// 2^31).
+void set_rope_turns(GatherKArgs& a, float base, int head_dim) {
+  for (int j = 0; j < 64; ++j) {
+    a.rope_turn[j] = 0ull;
+    if (base > 0.f && j < head_dim / 2) {
+      const double g = std::pow((double)base, -2.0 * j / head_dim) / 6.283185307179586;
+      a.rope_turn[j] = (unsigned long long)std::llround(std::ldexp(g, 64));
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
@@ -172,97 +188,148 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
   (void)lt;
 }
 
-// One warp per compact row.
+// Packed pairs of fp32 and their conversion to a bf16 pair.
+DS_DEV uint64_t f2pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+DS_DEV uint32_t bf16x2_of(uint64_t v) {   // round each half to bf16, low in bits 0..15
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+DS_DEV uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+DS_DEV uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+DS_DEV uint64_t fneg2(uint64_t a) { return a ^ 0x8000000080000000ull; }
+
 // One compact row: source token (page pg, offset off) of every kv head into
 // compact row (b, i), K rotated to local position i when rope_base > 0 (the
-// whole warp calls it; pg < 0 writes zeros).
+// whole warp calls it; pg < 0 writes zeros).  `cs` is the warp's scratch of
+// D/2 (cos, sin) pairs in shared memory.
+template <int D>
 DS_DEV void put_row(const GatherKArgs& a, const int b, const int i, const int pg,
-                    const int off) {
+                    const int off, float2* cs) {
+  constexpr int VPH = D / 8;                          // 16-byte vectors per head
+  constexpr int HALF = D / 2;
+  constexpr int NB = HALF / 8;                        // K units (8 pairs) per head
   const int lane = threadIdx.x & 31;
-  const int vec_per_head = a.head_dim / 8;            // 16-byte vectors
-  const int nvec = a.num_kv_heads * vec_per_head;
-  const int64_t drow = ((int64_t)b * a.capacity + i) * a.num_kv_heads * a.head_dim;
+  const int nvec = a.num_kv_heads * VPH;
+  const int64_t drow = ((int64_t)b * a.capacity + i) * a.num_kv_heads * D;
   const int64_t srow = (int64_t)pg * a.page_stride + (int64_t)off * a.tok_stride;
-  const bool rope = a.rope_base > 0.f;
-  for (int e = lane; e < nvec; e += 32) {
-    const int h = e / vec_per_head, vv = e % vec_per_head;
-    uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
-    if (pg >= 0) {
-      const int64_t so = srow + (int64_t)h * a.head_stride + vv * 8;
-      if (!rope) kx = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
-      vx = __ldg(reinterpret_cast<const uint4*>(a.src_v + so));
-    }
-    if (!rope) reinterpret_cast<uint4*>(a.out_k + drow)[e] = kx;
-    reinterpret_cast<uint4*>(a.out_v + drow)[e] = vx;
-  }
-  if (!rope) return;
-
-  // K rotated to local position i.  The angle i * base^(-2j/D) is formed and
-  // reduced modulo 2 pi in float64 (positions reach tens of thousands of
-  // radians), then its sine and cosine are taken in float32 and the pair
-  // (j, j + D/2) rotated in float32 and rounded to bf16.  Lane l holds the
-  // sine and cosine of pairs l and l + 32.
-  const int half = a.head_dim / 2;
-  float cq[2], sq[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int j = lane + 32 * q;
-    cq[q] = 1.f;
-    sq[q] = 0.f;
-    if (j < half) {
-      const double ang = (double)i * a.inv_freq[j];
-      const double k = rint(ang * 0.15915494309189535);           // 1 / (2 pi)
-      const float r = (float)fma(-k, 6.283185307179586, ang);      // in [-pi, pi]
-      sincosf(r, &sq[q], &cq[q]);
-    }
-  }
-  // units of (kv head, block of 8 pairs), the whole warp in step so that
-  // every lane takes part in every shuffle
-  const int nb = half / 8;
-  const int units = a.num_kv_heads * nb;
-  for (int u0 = 0; u0 < units; u0 += 32) {
-    const int u = u0 + lane;
-    const bool valid = u < units;
-    const int h = valid ? u / nb : 0, j0 = valid ? (u % nb) * 8 : 0;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (valid && pg >= 0) {
-      const int64_t so = srow + (int64_t)h * a.head_stride + j0;
-      lo = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
-      hi = __ldg(reinterpret_cast<const uint4*>(a.src_k + so + half));
-    }
-    const uint32_t* lw = reinterpret_cast<const uint32_t*>(&lo);
-    const uint32_t* hw = reinterpret_cast<const uint32_t*>(&hi);
-    uint32_t ow_lo[4], ow_hi[4];
-#pragma unroll
-    for (int e2 = 0; e2 < 4; ++e2) {
-      float xo[2], yo[2];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int j = j0 + 2 * e2 + p;
-        const float c0 = __shfl_sync(0xffffffffu, cq[0], j & 31);
-        const float c1 = __shfl_sync(0xffffffffu, cq[1], j & 31);
-        const float s0 = __shfl_sync(0xffffffffu, sq[0], j & 31);
-        const float s1 = __shfl_sync(0xffffffffu, sq[1], j & 31);
-        const float c = j < 32 ? c0 : c1, sn = j < 32 ? s0 : s1;
-        const float x = __uint_as_float((p ? (lw[e2] >> 16) : (lw[e2] & 0xffffu)) << 16);
-        const float y = __uint_as_float((p ? (hw[e2] >> 16) : (hw[e2] & 0xffffu)) << 16);
-        xo[p] = fmaf(x, c, -y * sn);
-        yo[p] = fmaf(x, sn, y * c);
+  if (!(a.rope_base > 0.f)) {
+    for (int e = lane; e < nvec; e += 32) {
+      const int h = e / VPH, vv = e % VPH;
+      uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
+      if (pg >= 0) {
+        const int64_t so = srow + (int64_t)h * a.head_stride + vv * 8;
+        kx = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
+        vx = __ldg(reinterpret_cast<const uint4*>(a.src_v + so));
       }
-      ow_lo[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xo[0])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xo[1])) << 16);
-      ow_hi[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yo[0])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(yo[1])) << 16);
+      reinterpret_cast<uint4*>(a.out_k + drow)[e] = kx;
+      reinterpret_cast<uint4*>(a.out_v + drow)[e] = vx;
     }
-    if (valid) {
-      uint16_t* dk = a.out_k + drow + (int64_t)h * a.head_dim + j0;
+    return;
+  }
+
+  // With RoPE, K goes in units of (kv head, block of 8 pairs (j, j + D/2)):
+  // 16 bytes from each half of the head.  Per round a lane loads four of the
+  // row's 16-byte V vectors and two K units together, so that the row costs
+  // one memory round trip, then writes V and rotates K.
+  //
+  // The angle i * base^(-2j/D) (positions reach tens of thousands of
+  // radians) is reduced modulo one turn exactly: with g_j the frequency as a
+  // 64-bit fraction of a turn (host-computed), i * g_j wraps modulo 2^64 to
+  // the angle's fraction of a turn, whose top 32 bits read as a signed
+  // number give x in [-1, 1) with angle = pi x (mod 2 pi).  Then sin and cos
+  // of pi x in float32 (lane l: pairs l and l + 32, shared with the warp
+  // through `cs`), the pair rotated in float32 and rounded to bf16.
+  const int units = a.num_kv_heads * NB;
+  for (int r = 0; 128 * r < nvec; ++r) {
+    uint4 vx[4], lo[2], hi[2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = 128 * r + 32 * k + lane;
+      vx[k] = make_uint4(0, 0, 0, 0);
+      if (e < nvec && pg >= 0) {
+        const int64_t so = srow + (int64_t)(e / VPH) * a.head_stride + (e % VPH) * 8;
+        vx[k] = __ldg(reinterpret_cast<const uint4*>(a.src_v + so));
+      }
+    }
+    int hh[2], jj[2];
+    bool valid[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int u = 64 * r + 32 * w + lane;
+      valid[w] = u < units;
+      hh[w] = u / NB;
+      jj[w] = (u % NB) * 8;
+      lo[w] = hi[w] = make_uint4(0, 0, 0, 0);
+      if (valid[w] && pg >= 0) {
+        const int64_t so = srow + (int64_t)hh[w] * a.head_stride + jj[w];
+        lo[w] = __ldg(reinterpret_cast<const uint4*>(a.src_k + so));
+        hi[w] = __ldg(reinterpret_cast<const uint4*>(a.src_k + so + HALF));
+      }
+    }
+    if (r == 0) {
+      __syncwarp();                 // the warp's previous row has read `cs`
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = lane + 32 * q;
+        if (j < HALF) {
+          const unsigned long long turn = (unsigned long long)(unsigned)i * a.rope_turn[j];
+          const float x = (float)(int)(turn >> 32) * 4.656612873077393e-10f;   // 2^-31
+          float sn, c;
+          sincospif(x, &sn, &c);
+          cs[j] = make_float2(c, sn);
+        }
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = 128 * r + 32 * k + lane;
+      if (e < nvec) reinterpret_cast<uint4*>(a.out_v + drow)[e] = vx[k];
+    }
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      if (!valid[w]) continue;
+      const int j0 = jj[w];
+      const uint32_t* lw = reinterpret_cast<const uint32_t*>(&lo[w]);
+      const uint32_t* hw = reinterpret_cast<const uint32_t*>(&hi[w]);
+      const float4* c4 = reinterpret_cast<const float4*>(cs + j0);   // pairs j0 .. j0 + 7
+      uint32_t ow_lo[4], ow_hi[4];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        // pairs j0 + 2 e2 and j0 + 2 e2 + 1: (cos, sin) of both in one load
+        const float4 t = c4[e2];
+        const uint64_t C = f2pk(t.x, t.z), S = f2pk(t.y, t.w);
+        const uint64_t X = f2pk(__uint_as_float(lw[e2] << 16), __uint_as_float(lw[e2] & 0xffff0000u));
+        const uint64_t Y = f2pk(__uint_as_float(hw[e2] << 16), __uint_as_float(hw[e2] & 0xffff0000u));
+        // x' = x cos - y sin, y' = x sin + y cos
+        ow_lo[e2] = bf16x2_of(ffma2(X, C, fneg2(fmul2(Y, S))));
+        ow_hi[e2] = bf16x2_of(ffma2(X, S, fmul2(Y, C)));
+      }
+      uint16_t* dk = a.out_k + drow + (int64_t)hh[w] * D + j0;
       *reinterpret_cast<uint4*>(dk) = make_uint4(ow_lo[0], ow_lo[1], ow_lo[2], ow_lo[3]);
-      *reinterpret_cast<uint4*>(dk + half) = make_uint4(ow_hi[0], ow_hi[1], ow_hi[2], ow_hi[3]);
+      *reinterpret_cast<uint4*>(dk + HALF) = make_uint4(ow_hi[0], ow_hi[1], ow_hi[2], ow_hi[3]);
     }
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
+  __shared__ __align__(16) float2 s_cs[8][D / 2];
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp;
@@ -292,7 +359,7 @@ __global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
     if (lane == 0) flag(a.status, DS_DEV_BAD_PAGE);
     pg = -1;
   }
-  put_row(a, b, i, pg, t % a.page_size);
+  put_row<D>(a, b, i, pg, t % a.page_size, s_cs[warp]);
 }
 
 cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
@@ -319,15 +386,15 @@ cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
   a.out_chunk_ids = g.out_chunk_ids;
   a.status = static_cast<uint32_t*>(g.workspace);
   a.rope_base = g.rope_base;
-  for (int j = 0; j < 64; ++j)
-    a.inv_freq[j] = (g.rope_base > 0.f && j < g.head_dim / 2)
-                        ? std::pow((double)g.rope_base, -2.0 * j / g.head_dim)
-                        : 0.0;
+  set_rope_turns(a, g.rope_base, g.head_dim);
   topk_select<<<g.batch, kSelThreads, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 grid((g.capacity + 7) / 8, g.batch);
-  gather_rows<<<grid, 256, 0, stream>>>(a);
+  if (g.head_dim == 128)
+    gather_rows<128><<<grid, 256, 0, stream>>>(a);
+  else
+    gather_rows<64><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -336,8 +403,10 @@ cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
 // tokens committed since are appended behind its last row (the rolling
 // window grows), K rotated to the appended rows' local positions.  One CTA
 // per sequence, one warp per appended token.
+template <int D>
 __global__ void __launch_bounds__(256) compact_append(GatherKArgs a) {
   __shared__ int s_n0, s_cnt;
+  __shared__ __align__(16) float2 s_cs[8][D / 2];
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -364,7 +433,7 @@ __global__ void __launch_bounds__(256) compact_append(GatherKArgs a) {
       pg = -1;
     }
     if (lane == 0) posrow[i] = t;
-    put_row(a, b, i, pg, t % a.page_size);
+    put_row<D>(a, b, i, pg, t % a.page_size, s_cs[warp]);
   }
   __syncthreads();
   if (threadIdx.x == 0 && cnt > 0) a.out_len[b] = n0 + cnt;
@@ -394,13 +463,13 @@ cudaError_t launch_compact_append(const ds_append_args& g, cudaStream_t stream) 
   a.out_len = g.out_len;
   a.status = static_cast<uint32_t*>(g.workspace);
   a.rope_base = g.rope_base;
-  for (int j = 0; j < 64; ++j)
-    a.inv_freq[j] = (g.rope_base > 0.f && j < g.head_dim / 2)
-                        ? std::pow((double)g.rope_base, -2.0 * j / g.head_dim)
-                        : 0.0;
+  set_rope_turns(a, g.rope_base, g.head_dim);
   a.from_lens = g.from_lens;
   a.to_lens = g.to_lens;
-  compact_append<<<g.batch, 256, 0, stream>>>(a);
+  if (g.head_dim == 128)
+    compact_append<128><<<g.batch, 256, 0, stream>>>(a);
+  else
+    compact_append<64><<<g.batch, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

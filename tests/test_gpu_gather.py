@@ -98,8 +98,9 @@ def test_gather_with_local_rope(layout, head_dim):
     """rope_base > 0: K rotated to its local position in the compact cache
     (vllm-diffspec README, "Architecture", dual-view draft cache).  Selection,
     positions, lengths and V stay byte-exact.  K against the oracle's
-    once-rounded float64 rotation: the kernel reduces the angle in float64
-    and rotates in float32, an absolute error of at most ~1e-6 of the pair's
+    once-rounded float64 rotation: the kernel reduces the angle exactly in
+    64-bit fixed point, rounds it to float32 (at most 2^-24 pi off) and
+    rotates in float32, an absolute error of at most ~1e-6 of the pair's
     norm before rounding, so |gpu - ref| <= ulp_bf16(ref) + 1e-6 * |pair|;
     and nearly every value is equal."""
     wl = synth.tiny_workload(batch=3, chunk_size=32, top_k=6, window=200,
