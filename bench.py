@@ -328,6 +328,99 @@ def code_sha256(src_path: str) -> str:
 
 
 # ---------------------------------------------------------------------------
+# the other workloads, measured in the same process after the headline
+
+OTHER_WORKLOADS = ("llama8b-32k", "llama8b-64k", "qwen3-8b-ragged-b8")
+OTHER_LAYERS = 4      # distinct layer caches per workload, rotated (> L2)
+
+
+def workload_block(name, dev, peak, reps=6):
+    """Split pass, whole verify call, retrieval and acceptance of one of the
+    other workloads: OTHER_LAYERS layers with their own caches are verified
+    back to back `reps` times; the split pass of every layer is bracketed by
+    CUDA events (per-call figures, so the dependent launch of the next call
+    is broken; the headline's own step is timed without that)."""
+    import torch
+    from long_context_speculative_ds_gb300 import binding, synth
+    from long_context_speculative_ds_gb300.step import StepInputs, VerifyStep
+    wl = synth.WORKLOADS[name]
+    nl = min(OTHER_LAYERS, wl.layers) if wl.layers > 1 else OTHER_LAYERS
+    st = synth.make_structure(wl)
+    qs, ks, vs = [], [], []
+    for l in range(nl):
+        q, k, v = synth.make_layer(st, l, device=dev)
+        qs.append(q); ks.append(k); vs.append(v)
+    sk, sv = synth.make_source_cache(st, device=dev)
+    mode = "reject" if wl.accept == "reject" else "greedy"
+    acc = synth.make_accept_inputs(st, mode, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    inp = StepInputs(page_table=st.page_table.to(dev),
+                     ctx_lens=torch.tensor(st.ctx_lens, **i32),
+                     tree_offsets=torch.tensor(st.tree_offsets, **i32),
+                     parents=torch.tensor(st.parents, **i32),
+                     q=qs, k_cache=ks, v_cache=vs, src_k=sk, src_v=sv,
+                     target_logits=acc.target_logits, draft_logits=acc.draft_logits,
+                     draft_tokens=acc.draft_tokens, uniforms=acc.uniforms)
+    step = VerifyStep(inp, chunk_size=wl.chunk_size, top_k=wl.top_k, window=wl.window,
+                      accept_mode=mode, rope_base=wl.rope_base)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nl)] for _ in range(reps)]
+    for e_a, e_b in (e for row in evs for e in row):   # torch creates them on first record
+        e_a.record()
+        e_b.record()
+    pargs = [[binding.verify_args(
+        inp.q[l], inp.k_cache[l], inp.v_cache[l], inp.page_table, inp.ctx_lens,
+        inp.tree_offsets, inp.parents, chunk_size=wl.chunk_size, out=step.out[l],
+        chunk_scores=step.scores, workspace=step.ws_verify, accumulate=l > 0,
+        prof_events=evs[r][l]) for l in range(nl)] for r in range(reps)]
+    for _ in range(3):
+        step.run()
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for r in range(reps):
+        for l in range(nl):
+            binding.ds_verify_attn(pargs[r][l])
+    c1.record()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    verify_us = c0.elapsed_time(c1) * 1e3 / (reps * nl)
+    split_us = statistics.median(a.elapsed_time(b) * 1e3 for row in evs for a, b in row)
+
+    def alone(fn, n=10):
+        fn()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(n):
+            fn()
+        a1.record()
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) * 1e3 / n
+    gather_us = alone(step.gather)
+    accept_us = alone(step.accept)
+    assert step.device_status() == 0
+    alg = _kv_bytes(wl, st) + _q_bytes(wl, st)
+    achieved = alg / (split_us * 1e-6) / 1e9
+    accept_bytes = st.n_nodes * wl.vocab * 4 * (2 if mode == "reject" else 1)
+    out = {
+        "batch": wl.batch, "ctx_lens": st.ctx_lens, "tree_nodes": st.tree_sizes,
+        "layers_rotated": nl,
+        "split_pass_us": round(split_us, 2),
+        "split_pass_gbs": round(achieved, 1),
+        "split_pass_frac": round(achieved / peak, 4),
+        "algorithmic_bytes_per_layer": alg,
+        "verify_call_us": round(verify_us, 2),
+        "verify_call_frac": round(alg / (verify_us * 1e-6) / 1e9 / peak, 4),
+        "retrieval_us": round(gather_us, 2),
+        "accept_us": round(accept_us, 2), "accept_mode": mode,
+        "accept_gbs": round(accept_bytes / (accept_us * 1e-6) / 1e9, 1),
+    }
+    del step, inp, qs, ks, vs, sk, sv, acc
+    torch.cuda.empty_cache()
+    return out
+
 
 def _end_to_end(step, inp, args, world, dev, barrier):
     """Per step: copy the step's inputs from pinned host memory (on a side
@@ -593,6 +686,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
     }
+    if not args.no_workloads and wl.name == DEFAULT_WORKLOAD:
+        del inp, step, qs, ks, vs, sk, sv, acc
+        torch.cuda.empty_cache()
+        line["workloads"] = {n: workload_block(n, dev, peak) for n in OTHER_WORKLOADS}
     if world == 1 and not args.no_cpu_baseline:
         n_cpu = min(CPU_BASELINE_LAYERS, wl.layers)
         cst, clayers, csrc, cacc = cpu_inputs(wl, n_cpu)
@@ -612,6 +709,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the 32K, 64K and ragged workloads' block")
     ap.add_argument("--kv-layout", choices=["NHD", "HND"], default="NHD")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the workload's layer count (profiling runs)")
