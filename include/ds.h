@@ -268,7 +268,9 @@ ds_status ds_chunk_topk_gather(const ds_gather_args* args, void* stream);
  *   uniforms[c][0] * q(x) < p(x); on rejection p <- max(0, p - q) /
  *   sum(max(0, p - q)) (p kept when that sum is 0).  An accepted child
  *   becomes the current node.  With no child accepted, the bonus token is
- *   the smallest x with sum_{y <= x} p(y) > uniforms[i][1] * sum(p).
+ *   the smallest x with sum_{y <= x} p(y) > uniforms[i][1] * sum(p).  A
+ *   draft token outside [0, vocab) at a non-root node sets DS_DEV_BAD_TOKEN
+ *   and that node is never accepted.
  *
  * Outputs: out_path[b, 0..n-1] = accepted local node ids in order (-1
  * padded to DS_MAX_TREE_NODES), out_n_accepted[b] = n, out_bonus[b].  A
@@ -304,9 +306,9 @@ ds_status ds_accept(const ds_accept_args* args, void* stream);
  *
  * Same arguments, kernels and results as ds_accept, except that
  * args->workspace must be NULL and args->workspace_bytes 0: the scratch
- * (a status word and one 112-byte record per tree node) is a fixed array in
+ * (a status word and one 96-byte record per tree node) is a fixed array in
  * device global memory inside the library, DS_ACCEPT_STATIC_MAX_NODES
- * records long (about 448 KiB per device).  Nothing is allocated, on the
+ * records long (384 KiB per device).  Nothing is allocated, on the
  * device or through any library, by this call.
  *
  * Refused with DS_ERR_UNSUPPORTED: args->n_nodes > DS_ACCEPT_STATIC_MAX_NODES

@@ -10,26 +10,29 @@
 //     its lowest index.
 // Rejection
 //   node pass (one cluster of 8 CTAs per tree node, each CTA one eighth of
-//     the vocabulary, partial results combined through distributed shared
-//     memory).  The CTA keeps its slice of the node's residual r in shared
-//     memory, so every vocabulary pass after the first reads it there:
+//     the vocabulary, partial sums pushed into every CTA of the cluster
+//     through distributed shared memory).  The CTA's slice of the target
+//     row arrives in shared memory by one bulk copy; an inner node's draft
+//     slice is loaded into registers at the same time.  Then:
 //       target max and sum exp(l - max), and the same for the draft;
-//       for the k-th child of the node the residual normaliser
-//         Z_k = sum_y max(0, r_{k-1}(y) - q(y)),  r_0 = p,
-//         r_k = max(0, r_{k-1} - q) / Z_k  (r_k = r_{k-1} when Z_k = 0),
-//       one pass per child (r updated in place), which does not depend on
-//       the children's tokens, so every node's residual chain is computed in
-//       parallel before the walk;
+//       p and q of the slice, in place;
+//       for the k-th child (k >= 1) the residual it is tested against, in
+//         closed form r_k = max(0, p - s_k q) / C_k with s_k = 1 + C_1 +
+//         ... + C_{k-1} and C_k = sum_y max(0, p - s_k q): one pass over the
+//         slice and one cluster sum per child; the chain does not depend on
+//         the children's tokens, so every node's chain runs in parallel
+//         before the walk;
 //       the bonus token the walk would draw if it stopped here: the smallest
-//       x with sum_{y<=x} r_m(y) > u * sum_y r_m(y), m = number of children.
+//         x with sum_{y<=x} r_m(y) > u * sum_y r_m(y), m = number of
+//         children, found by the one CTA whose slice holds the threshold.
 //     A leaf needs only its target row (its draft row is never read).
-//     Per-element values are fp32; sums are compensated fp32 pairs, added in
-//     float64 only across the cluster's eight CTAs.  Vocabularies whose slice would not fit in
-//     shared memory use a streaming variant that recomputes p, q and the
-//     chain from the logits on every pass.
+//     Per-element values are fp32; sums are compensated fp32 pairs.
+//     Vocabularies whose slice would not fit in registers and shared memory
+//     (or rows that are not 16-byte aligned) use a streaming variant that
+//     recomputes p and q from the logits on every pass.
 // walk (one warp per sequence): follows the tree from the root.  Greedy
 //   compares draft tokens with the argmax; rejection evaluates p(x), q(x) and
-//   the residual chain at the proposed token with the node pass's own fp32
+//   the proposed child's residual r(x) with the node pass's own fp32
 //   operations and stored scalars, and tests u * q(x) < r(x).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -39,6 +42,7 @@
 #include "dev_common.cuh"
 #include "internal.h"
 #include "pdl.cuh"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -48,8 +52,6 @@ constexpr int kAccCluster = 8;
 constexpr int kAccThreads = 512;
 constexpr int kAccWarps = kAccThreads / 32;
 constexpr int kArgThreads = 256;
-// largest shared-memory slice (floats) of the in-shared-memory rejection pass
-constexpr int kRejMaxSlice = 40 * 1024;
 
 struct AcceptKArgs {
   int32_t mode;
@@ -89,22 +91,6 @@ DS_DEV int seq_of(const int32_t* offsets, int batch, int node) {
     if (__ldg(offsets + mid) <= node) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-// Children of `node` in increasing local index (thread 0 of the block).  A
-// malformed tree (flagged by the walk) gets no children, so no parent read
-// leaves the node arrays.  Returns the sequence's first node.
-DS_DEV int find_children(const AcceptKArgs& a, int node, int32_t* children, int* nch) {
-  const int b = seq_of(a.offsets, a.batch, node);
-  const int n0 = __ldg(a.offsets + b);
-  int T = __ldg(a.offsets + b + 1) - n0;
-  if (T > DS_MAX_TREE_NODES || T < 0 || n0 < 0 || n0 + T > a.n_nodes) T = 0;
-  int n = 0;
-  const int i = node - n0;
-  for (int c = i + 1; c < T; ++c)
-    if (__ldg(a.parents + n0 + c) == i) children[n++] = c;
-  *nch = n;
-  return n0;
 }
 
 // Key whose unsigned order is (logit ascending, then index descending).
@@ -170,13 +156,25 @@ __global__ void __launch_bounds__(kArgThreads) accept_argmax(AcceptKArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// rejection: node pass with the residual slice in shared memory
+// rejection: node pass, target slice in shared memory, draft slice in registers
 //
-// FP64 throughput on this part is a small fraction of FP32, so per-element
-// and per-thread work stays in fp32: sums are Kahan-compensated per thread
-// and combined as unevaluated pairs (hi, lo) with error-free two-sums; only
-// the eight per-CTA pairs of a cluster are added in float64, by one warp,
-// and the derived scalars (1 / S, 1 / Z) are formed once and broadcast.
+// FP64 throughput on this part is a small fraction of FP32, so the node pass
+// computes in fp32 only: per-thread sums are Kahan-compensated and combined
+// as unevaluated pairs (hi, lo) with error-free two-sums.  The eight CTAs of
+// a cluster push their partial pairs into every CTA of the cluster and meet
+// at one cluster barrier; every thread of every CTA then adds the same eight
+// pairs in the same order, so all CTAs derive bit-identical scalars (maxima,
+// 1 / S, the chain's s_k and 1 / C_k) without a broadcast.
+//
+// Residual chain in closed form.  With C_0 = 1, s_k = C_0 + ... + C_{k-1}
+// and R_k = max(0, p - s_k q), C_k = sum_y R_k(y), the residual after k
+// rejected siblings is r_k = R_k / C_k: by induction, max(0, r_{k-1} - q)
+// = max(0, R_{k-1} - C_{k-1} q) / C_{k-1}, and where R_{k-1} > 0 that is
+// (p - s_k q) / C_{k-1} while where R_{k-1} = 0 both sides vanish (p <= s_{k-1} q
+// <= s_k q); normalising gives R_k / C_k.  So each child costs one pass of
+// max(0, p - s q) over the slice and one cluster sum, never a replay of the
+// earlier steps, and no per-element state changes between passes.  A zero
+// residual (C_k = 0) keeps r_{k-1}, and then every later residual too.
 
 // hi + lo, |lo| small against hi
 struct F2 {
@@ -199,135 +197,98 @@ DS_DEV F2 f2_shfl_xor(F2 x, int o) {
 DS_DEV F2 f2_shfl_up(F2 x, int o) {
   return {__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
 }
+DS_DEV F2 f2_shfl(F2 x, int src) {
+  return {__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
+}
 DS_DEV F2 kahan_f2(const Kahan& k) { return {k.s, -k.c}; }
-// F2 of a double (hi = nearest float, lo = the rest rounded)
-DS_DEV F2 f2_of(double x) {
-  const float hi = (float)x;
-  return {hi, (float)(x - (double)hi)};
-}
-// x > y for F2 values
-DS_DEV bool f2_gt(F2 x, F2 y) {
-  const F2 d = f2_add(x, F2{-y.hi, -y.lo});
-  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
-}
-
-// Running (max, sum of exp(x - max)) of one thread, the sum compensated.
-struct OnlineExp {
-  float m;
-  Kahan k;
-  DS_DEV OnlineExp() : m(-__builtin_inff()) {}
-  // adds four values: rescales when the maximum moves (rarely after the
-  // first values), then adds their exponentials as one pairwise partial sum
-  DS_DEV void add4(float4 x) {
-    const float m4 = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-    if (m4 > m) {
-      const float f = m == -CUDART_INF_F ? 0.f : expf(m - m4);
-      k.s *= f;
-      k.c *= f;
-      m = m4;
-    }
-    if (m == -CUDART_INF_F) return;
-    k.add((expf(x.x - m) + expf(x.y - m)) + (expf(x.z - m) + expf(x.w - m)));
-  }
-  DS_DEV void add1(float x) { add4(make_float4(x, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F)); }
-};
-
-struct RejShared {
-  F2 part[2][2];               // cluster slots (two values), used alternately
-  float pmax[2][2];            // maxima beside part (online exponential sums)
-  F2 red[kAccWarps][2];
-  float redm[kAccWarps][2];
-  double dres[2];              // cluster results, float64
-  double dpre, dmine;          // value 0: partials of the CTAs before this one,
-                               // and this CTA's (see rank_split)
-  double btot, bpre, bmine;    // the same for the bonus draw's weights
-  float fres[4];               // scalars derived by thread 0
-  F2 scan[kAccWarps + 1];
-  int32_t first;
-  int32_t children[DS_MAX_TREE_NODES];
-  int32_t nch, n0, bonus;
-};
-
+// x * f with the product's rounding error kept
 DS_DEV F2 f2_scale(F2 x, float f) {
   const float hi = x.hi * f;
   return {hi, fmaf(x.hi, f, -hi) + x.lo * f};
 }
-
-// Warp 0, lane k holding CTA k's partial d of a cluster sum: stores this
-// CTA's partial and the sum of the partials of the CTAs before it (the
-// slice's offset in vocabulary order).
-DS_DEV void rank_split(RejShared& sh, unsigned rank, double d) {
-  const int lane = threadIdx.x & 31;
-  const double mine = __shfl_sync(0xffffffffu, d, rank);
-  double pre = lane < (int)rank ? d : 0.0;
-  for (int o = 4; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
-  if (lane == 0) { sh.dpre = pre; sh.dmine = mine; }
+// x <= y for F2 values
+DS_DEV bool f2_le(F2 x, F2 y) {
+  const F2 d = f2_add(y, F2{-x.hi, -x.lo});
+  return d.hi > 0.f || (d.hi == 0.f && d.lo >= 0.f);
 }
+DS_DEV bool f2_gt(F2 x, F2 y) { return !f2_le(x, y); }
+// 1 / x of a positive pair, in fp32 (one Newton step on the pair)
+DS_DEV float recip_f2(F2 x) {
+  const float r = 1.0f / x.hi;
+  const float e = fmaf(-x.hi, r, 1.0f) - x.lo * r;
+  return fmaf(r, e, r);
+}
+constexpr int kRejMaxG = 10;   // 16-byte groups per thread held in registers
 
-// Cluster reduction of two compensated sums: every thread passes its pair;
-// afterwards sh.dres[0..1] (float64) hold the totals over the cluster.  One
-// cluster barrier per call: the slot written alternates between calls, and
-// a CTA writes a slot again only after every CTA has passed the barrier of
-// the call in between.
-DS_DEV void cluster_sum2(cg::cluster_group& cl, RejShared& sh, int& slot, F2 x0, F2 x1) {
+struct RejShared {
+  uint64_t bar;                                // target slice copy
+  F2 part[2][kAccCluster][2];                  // pushed CTA partials [slot][rank][value]
+  float pmax[2][kAccCluster][2];               // their maxima (online sums)
+  F2 red[kAccWarps][2];
+  float redm[kAccWarps][2];
+  float rsum[kAccWarps][kRejMaxG];             // bonus scan: warp sums per round
+  F2 rtot[kRejMaxG];                           // bonus scan: round totals
+  F2 wtot[kAccWarps];                          // bonus scan: warp totals of one round
+  int32_t children[DS_MAX_TREE_NODES];
+  int32_t first, pick;
+  int32_t stop, inner;                         // finish: the walk's stop node
+};
+
+// Block + cluster sum of one compensated value per thread.  Returns the
+// cluster total; sh.part[slot][r][0] holds CTA r's partial afterwards (until
+// the reduction after next reuses the slot).  A CTA writes slot s again only
+// after every CTA has passed the barrier of the reduction in between, by
+// which time every thread has finished reading slot s.
+DS_DEV F2 cluster_sum(cg::cluster_group& cl, RejShared& sh, int& slot, F2 x) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int o = 16; o > 0; o >>= 1) {
-    x0 = f2_add(x0, f2_shfl_xor(x0, o));
-    x1 = f2_add(x1, f2_shfl_xor(x1, o));
-  }
-  if (lane == 0) { sh.red[warp][0] = x0; sh.red[warp][1] = x1; }
+  const unsigned rank = cl.block_rank();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = f2_add(x, f2_shfl_xor(x, o));
+  if (lane == 0) sh.red[warp][0] = x;
   __syncthreads();
   if (warp == 0) {
-    F2 a0 = lane < kAccWarps ? sh.red[lane][0] : F2{0.f, 0.f};
-    F2 a1 = lane < kAccWarps ? sh.red[lane][1] : F2{0.f, 0.f};
-    for (int o = 8; o > 0; o >>= 1) {
-      a0 = f2_add(a0, f2_shfl_xor(a0, o));
-      a1 = f2_add(a1, f2_shfl_xor(a1, o));
-    }
-    if (lane == 0) { sh.part[slot][0] = a0; sh.part[slot][1] = a1; }
+    F2 y = lane < kAccWarps ? sh.red[lane][0] : F2{0.f, 0.f};
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) y = f2_add(y, f2_shfl_xor(y, o));
+    y = f2_shfl(y, 0);   // one value, pushed to every CTA
+    if (lane < kAccCluster) *cl.map_shared_rank(&sh.part[slot][rank][0], lane) = y;
   }
   cl.sync();
-  if (warp == 0) {
-    double d0 = 0.0, d1 = 0.0;
-    if (lane < kAccCluster) {
-      const F2* o = cl.map_shared_rank(&sh.part[slot][0], lane);
-      const F2 p0 = o[0], p1 = o[1];
-      d0 = (double)p0.hi + (double)p0.lo;
-      d1 = (double)p1.hi + (double)p1.lo;
-    }
-    rank_split(sh, cl.block_rank(), d0);
-    for (int o = 4; o > 0; o >>= 1) {
-      d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-      d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-    }
-    if (lane == 0) { sh.dres[0] = d0; sh.dres[1] = d1; }
-  }
+  F2 tot{0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kAccCluster; ++k) tot = f2_add(tot, sh.part[slot][k][0]);
   slot ^= 1;
+  return tot;
 }
 
-// The same for two online exponential sums (max, sum of exp(x - max)):
-// afterwards sh.fres[0..1] hold the maxima and sh.dres[0..1] the sums
-// relative to them.
-DS_DEV void cluster_online2(cg::cluster_group& cl, RejShared& sh, int& slot, float m0, F2 s0,
-                            float m1, F2 s1) {
+// The same for two online exponential sums (max, sum of exp(x - max)) per
+// thread: maxima first (warp, then block), every partial rescaled once to its
+// group's maximum, then compensated sums.  Returns the cluster maxima and
+// sums; sh.part/pmax[slot] keep the CTA partials of value 0 for bonus_owner.
+DS_DEV F2 rescale_to(F2 s, float m, float to) {
+  if (m == to) return s;
+  return m == -CUDART_INF_F ? F2{0.f, 0.f} : f2_scale(s, expf(m - to));
+}
+DS_DEV void cluster_online(cg::cluster_group& cl, RejShared& sh, int& slot, float& m0, F2& s0,
+                           float& m1, F2& s1) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto merge = [](float& m, F2& s, float om, F2 os) {
-    const float nm = fmaxf(m, om);
-    if (nm == -CUDART_INF_F) return;
-    s = f2_add(f2_scale(s, m == nm ? 1.f : expf(m - nm)),
-               f2_scale(os, om == nm ? 1.f : expf(om - nm)));
-    m = nm;
-  };
+  const unsigned rank = cl.block_rank();
+  float w0 = m0, w1 = m1;
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float om0 = __shfl_xor_sync(0xffffffffu, m0, o);
-    const float om1 = __shfl_xor_sync(0xffffffffu, m1, o);
-    const F2 os0 = f2_shfl_xor(s0, o), os1 = f2_shfl_xor(s1, o);
-    merge(m0, s0, om0, os0);
-    merge(m1, s1, om1, os1);
+    w0 = fmaxf(w0, __shfl_xor_sync(0xffffffffu, w0, o));
+    w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, o));
+  }
+  s0 = rescale_to(s0, m0, w0);
+  s1 = rescale_to(s1, m1, w1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s0 = f2_add(s0, f2_shfl_xor(s0, o));
+    s1 = f2_add(s1, f2_shfl_xor(s1, o));
   }
   if (lane == 0) {
     sh.red[warp][0] = s0; sh.red[warp][1] = s1;
-    sh.redm[warp][0] = m0; sh.redm[warp][1] = m1;
+    sh.redm[warp][0] = w0; sh.redm[warp][1] = w1;
   }
   __syncthreads();
   if (warp == 0) {
@@ -337,340 +298,397 @@ DS_DEV void cluster_online2(cg::cluster_group& cl, RejShared& sh, int& slot, flo
       a0 = sh.redm[lane][0]; a1 = sh.redm[lane][1];
       b0 = sh.red[lane][0]; b1 = sh.red[lane][1];
     }
+    float c0 = a0, c1 = a1;
+#pragma unroll
     for (int o = 8; o > 0; o >>= 1) {
-      const float om0 = __shfl_xor_sync(0xffffffffu, a0, o);
-      const float om1 = __shfl_xor_sync(0xffffffffu, a1, o);
-      const F2 os0 = f2_shfl_xor(b0, o), os1 = f2_shfl_xor(b1, o);
-      merge(a0, b0, om0, os0);
-      merge(a1, b1, om1, os1);
+      c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, o));
+      c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, o));
     }
-    if (lane == 0) {
-      sh.part[slot][0] = b0; sh.part[slot][1] = b1;
-      sh.pmax[slot][0] = a0; sh.pmax[slot][1] = a1;
+    b0 = rescale_to(b0, a0, c0);
+    b1 = rescale_to(b1, a1, c1);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      b0 = f2_add(b0, f2_shfl_xor(b0, o));
+      b1 = f2_add(b1, f2_shfl_xor(b1, o));
+    }
+    b0 = f2_shfl(b0, 0);   // one value, pushed to every CTA (the maxima are
+    b1 = f2_shfl(b1, 0);   // exact, so already equal in every lane)
+    if (lane < kAccCluster) {
+      F2* dp = cl.map_shared_rank(&sh.part[slot][rank][0], lane);
+      float* dm = cl.map_shared_rank(&sh.pmax[slot][rank][0], lane);
+      dp[0] = b0; dp[1] = b1;
+      dm[0] = c0; dm[1] = c1;
     }
   }
   cl.sync();
-  if (warp == 0) {
-    float mm0 = -CUDART_INF_F, mm1 = -CUDART_INF_F;
-    F2 p0{0.f, 0.f}, p1{0.f, 0.f};
-    if (lane < kAccCluster) {
-      const F2* o = cl.map_shared_rank(&sh.part[slot][0], lane);
-      const float* om = cl.map_shared_rank(&sh.pmax[slot][0], lane);
-      p0 = o[0]; p1 = o[1];
-      mm0 = om[0]; mm1 = om[1];
-    }
-    float M0 = mm0, M1 = mm1;
-    for (int o = 4; o > 0; o >>= 1) {
-      M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, o));
-      M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, o));
-    }
-    // each CTA's sum rescaled to the cluster maximum, added in float64
-    double d0 = 0.0, d1 = 0.0;
-    if (lane < kAccCluster) {
-      if (mm0 != -CUDART_INF_F) d0 = ((double)p0.hi + (double)p0.lo) * (double)expf(mm0 - M0);
-      if (mm1 != -CUDART_INF_F) d1 = ((double)p1.hi + (double)p1.lo) * (double)expf(mm1 - M1);
-    }
-    rank_split(sh, cl.block_rank(), d0);
-    for (int o = 4; o > 0; o >>= 1) {
-      d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-      d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-    }
-    if (lane == 0) {
-      sh.dres[0] = d0; sh.dres[1] = d1;
-      sh.fres[0] = M0; sh.fres[1] = M1;
-    }
+  float M0 = -CUDART_INF_F, M1 = -CUDART_INF_F;
+#pragma unroll
+  for (int k = 0; k < kAccCluster; ++k) {
+    M0 = fmaxf(M0, sh.pmax[slot][k][0]);
+    M1 = fmaxf(M1, sh.pmax[slot][k][1]);
   }
+  F2 S0{0.f, 0.f}, S1{0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kAccCluster; ++k) {
+    S0 = f2_add(S0, rescale_to(sh.part[slot][k][0], sh.pmax[slot][k][0], M0));
+    S1 = f2_add(S1, rescale_to(sh.part[slot][k][1], sh.pmax[slot][k][1], M1));
+  }
+  m0 = M0; s0 = S0; m1 = M1; s1 = S1;
   slot ^= 1;
 }
 
-// 1 / x of a positive float64 total, in fp32 arithmetic (the value is a
-// scalar that node pass and walk share; it need not be correctly rounded)
-DS_DEV float recip_f(double x) {
-  const float hi = (float)x;
-  const float lo = (float)(x - (double)hi);
-  const float r = 1.0f / hi;
-  return fmaf(-r * lo, r, r);
+// The CTA whose slice holds the bonus draw's threshold thr = u * total: the
+// largest rank r whose prefix P_r (sum of the partials of ranks < r, added in
+// rank order) is <= thr.  Every CTA evaluates the same pairs in the same
+// order, so exactly one claims the draw.  `online` selects the partials of
+// value 0 of an online reduction, rescaled to its maximum M.
+// Returns thr - P_owner through thr_rel.
+DS_DEV int bonus_owner(const RejShared& sh, int slot, bool online, float M, float u, F2& thr_rel) {
+  auto part = [&](int k) {
+    const F2 v = sh.part[slot][k][0];
+    if (!online) return v;
+    return rescale_to(v, sh.pmax[slot][k][0], M);
+  };
+  F2 tot{0.f, 0.f};
+#pragma unroll 1
+  for (int k = 0; k < kAccCluster; ++k) tot = f2_add(tot, part(k));
+  const F2 thr = f2_scale(tot, u);
+  F2 pre{0.f, 0.f};
+  int owner = 0;
+  F2 rel = thr;
+#pragma unroll 1
+  for (int k = 0; k < kAccCluster; ++k) {
+    if (f2_le(pre, thr)) { owner = k; rel = f2_add(thr, F2{-pre.hi, -pre.lo}); }
+    pre = f2_add(pre, part(k));
+  }
+  thr_rel = rel;
+  return owner;
 }
 
-// One pass over this CTA's slice: f(r, d) for every token, r the slice value
-// (updated in place) and d the token's draft logit (0 when need_d is
-// false).  Thread t takes the 16-byte groups t, t + kAccThreads, ... (the
-// same tokens in every pass), four groups at a time so that four 16-byte
-// loads of the draft row are in flight per thread.  f returns the value the
-// thread adds to its compensated sum; four tokens' values are added
-// pairwise first.
-template <class F>
-DS_DEV Kahan visit(const float* __restrict__ drow, float* r_s, int n, bool vec, bool need_d,
-                   F f) {
-  const int tid = threadIdx.x;
-  Kahan acc;
-  if (vec) {
-    const int n4 = n >> 2;
-    const float4* d4 = reinterpret_cast<const float4*>(drow);
-    float4* r4 = reinterpret_cast<float4*>(r_s);
-    for (int base = tid; base < n4; base += 4 * kAccThreads) {
-      float4 dv[4];
+DS_DEV bool bulk_wait(uint32_t bar) {
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, 0))
+    if (clock64() - t0 > (1ll << 31)) return false;
+  return true;
+}
+
+// Smallest slice index x with sum_{y <= x} w(y) > thr (slice order), w the
+// bonus weight of this node: thread t holds the 16-byte groups t + j *
+// kAccThreads, so round j is slice tokens [4 * kAccThreads * j, 4 *
+// kAccThreads * (j + 1)) in thread order.  Round totals first (warp sums,
+// then compensated sums over the warps), the round that crosses the
+// threshold next, then a block scan of that round.  When rounding leaves the
+// threshold past everything, the last token of positive weight.  Owner CTA
+// only; returns the slice index (or -1 for an empty slice).
+template <int G, class W>
+DS_DEV int bonus_scan(RejShared& sh, int n4, F2 thr_rel, W weight) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // ---- round totals
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = base + u * kAccThreads;
-        dv[u] = (need_d && e < n4) ? __ldg(d4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = base + u * kAccThreads;
-        if (e < n4) {
-          float4 x = r4[e];
-          const float a0 = f(x.x, dv[u].x), a1 = f(x.y, dv[u].y);
-          const float a2 = f(x.z, dv[u].z), a3 = f(x.w, dv[u].w);
-          r4[e] = x;
-          acc.add((a0 + a1) + (a2 + a3));
-        }
-      }
+  for (int j = 0; j < G; ++j) {
+    const int e = tid + j * kAccThreads;
+    float v = 0.f;
+    if (e < n4) {
+      const float4 w = weight(j, e);
+      v = (w.x + w.y) + (w.z + w.w);
     }
-  } else {
-    for (int e = tid; e < n; e += kAccThreads) {
-      float x = r_s[e];
-      acc.add(f(x, need_d ? __ldg(drow + e) : 0.f));
-      r_s[e] = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sh.rsum[warp][j] = v;
+  }
+  if (tid == 0) { sh.first = 0x7fffffff; sh.pick = -1; }
+  __syncthreads();
+  if (warp < G) {
+    F2 y{lane < kAccWarps ? sh.rsum[lane][warp] : 0.f, 0.f};
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) y = f2_add(y, f2_shfl_xor(y, o));
+    if (lane == 0) sh.rtot[warp] = y;
+  }
+  __syncthreads();
+  // ---- the round that crosses (every thread, the same arithmetic)
+  int js = -1, jlast = -1;
+  F2 base{0.f, 0.f};
+  {
+    F2 run{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const F2 rt = sh.rtot[j];
+      const F2 nxt = f2_add(run, rt);
+      if (js < 0 && f2_gt(nxt, thr_rel)) { js = j; base = run; }
+      if (rt.hi > 0.f) jlast = j;
+      run = nxt;
     }
   }
-  return acc;
+  const bool last_mode = js < 0;
+  if (last_mode) js = jlast;
+  if (js < 0) return n4 > 0 ? 4 * n4 - 1 : -1;   // no positive weight at all
+  // ---- this thread's four weights of round js
+  const int e = tid + js * kAccThreads;
+  float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+    if (j == js && e < n4) w = weight(j, e);
+  const int x0 = 4 * e;
+  if (!last_mode) {
+    const F2 own = two_sum(w.x + w.y, w.z + w.w);
+    F2 incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const F2 y = f2_shfl_up(incl, o);
+      if (lane >= o) incl = f2_add(incl, y);
+    }
+    if (lane == 31) sh.wtot[warp] = incl;
+    __syncthreads();
+    F2 pre = base;
+    for (int k = 0; k < warp; ++k) pre = f2_add(pre, sh.wtot[k]);
+    const F2 incl_all = f2_add(pre, incl);
+    if (e < n4 && f2_gt(incl_all, thr_rel)) atomicMin(&sh.first, tid);
+    __syncthreads();
+    if (tid == sh.first) {
+      F2 run = f2_add(incl_all, F2{-own.hi, -own.lo});
+      const float wv[4] = {w.x, w.y, w.z, w.w};
+      int pick = -1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        run = f2_add(run, F2{wv[q], 0.f});
+        if (pick < 0 && f2_gt(run, thr_rel)) pick = x0 + q;
+      }
+      if (pick < 0) pick = x0 + 3;
+      sh.pick = pick;
+    }
+    __syncthreads();
+    if (sh.pick >= 0) return sh.pick;
+  }
+  // rounding left the threshold past the round: its last token of positive weight
+  if (e < n4) {
+    int lastpos = -1;
+    if (w.x > 0.f) lastpos = x0;
+    if (w.y > 0.f) lastpos = x0 + 1;
+    if (w.z > 0.f) lastpos = x0 + 2;
+    if (w.w > 0.f) lastpos = x0 + 3;
+    if (lastpos >= 0) atomicMax(&sh.pick, lastpos);
+  }
+  __syncthreads();
+  return sh.pick;
 }
 
+DS_DEV float4 expf4(float4 x, float m) {
+  return make_float4(expf(x.x - m), expf(x.y - m), expf(x.z - m), expf(x.w - m));
+}
+DS_DEV float max4(float4 x) { return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)); }
+// max(0, p - s q) per element
+DS_DEV float4 resid4(float4 p, float4 q, float s) {
+  return make_float4(fmaxf(0.f, fmaf(-s, q.x, p.x)), fmaxf(0.f, fmaf(-s, q.y, p.y)),
+                     fmaxf(0.f, fmaf(-s, q.z, p.z)), fmaxf(0.f, fmaf(-s, q.w, p.w)));
+}
+DS_DEV float sum4(float4 x) { return (x.x + x.y) + (x.z + x.w); }
+
+// The CTA's slice of a node's rows: [v0, v1), n4 16-byte groups.
+struct Slice {
+  int v0, v1, n4;
+};
+DS_DEV Slice slice_of(int V, int rank) {
+  const int per = ((V + kAccCluster - 1) / kAccCluster + 3) & ~3;
+  Slice sl;
+  sl.v0 = min(V, rank * per);
+  sl.v1 = min(V, sl.v0 + per);
+  sl.n4 = (sl.v1 - sl.v0) >> 2;
+  return sl;
+}
+
+// Thread 0: the target slice of row `row` into shared memory by one bulk
+// copy that completes on `bar`.
+DS_DEV void copy_target_slice(const AcceptKArgs& a, int row, const Slice& sl, float4* dst,
+                              uint32_t bar) {
+  if (threadIdx.x != 0 || sl.n4 == 0) return;
+  const uint32_t bytes = (uint32_t)sl.n4 * 16u;
+  ptx::mbar_arrive_expect_tx(bar, bytes);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(ptx::smem_addr(dst)), "l"(a.tl + (int64_t)row * a.vocab + sl.v0), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Every thread: wait for the target slice (bounded; on a timeout the status
+// records it and the copy is waited for once more before the data is used).
+DS_DEV void wait_target_slice(const AcceptKArgs& a, const Slice& sl, uint32_t bar) {
+  if (sl.n4 > 0 && !bulk_wait(bar)) {
+    if (threadIdx.x == 0) flag(a.status, DS_DEV_TIMEOUT);
+    ptx::drain_wait(bar, 0);
+  }
+}
+
+// The draft slice of row `row` into registers, every load in flight at once
+// (-inf outside the slice, or everywhere when `load` is false).
+template <int G>
+DS_DEV void load_draft_slice(const AcceptKArgs& a, int row, const Slice& sl, bool load,
+                             float4 (&qv)[G]) {
+  const float4* drow = reinterpret_cast<const float4*>(a.dl + (int64_t)row * a.vocab + sl.v0);
+  const float4 ninf = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int e = (int)threadIdx.x + j * kAccThreads;
+    qv[j] = (load && e < sl.n4) ? __ldcs(drow + e) : ninf;
+  }
+}
+
+// Per-thread (max, compensated sum of exp(x - max)) over the thread's groups
+// of the shared slice.
+template <int G>
+DS_DEV void thread_online_smem(const float4* p_s, int n4, float& m, F2& s) {
+  m = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int e = (int)threadIdx.x + j * kAccThreads;
+    if (e < n4) m = fmaxf(m, max4(p_s[e]));
+  }
+  Kahan k;
+  if (m != -CUDART_INF_F) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int e = (int)threadIdx.x + j * kAccThreads;
+      if (e < n4) k.add(sum4(expf4(p_s[e], m)));
+    }
+  }
+  s = kahan_f2(k);
+}
+
+// One cluster of kAccCluster CTAs per tree node; CTA `rank` owns the slice
+// [v0, v1) of the vocabulary, at most 4 * kAccThreads * G tokens.  Needs
+// 16-byte aligned rows (vocab % 4 == 0).  A leaf leaves at once: its
+// distribution matters only if the walk stops there, and then the finish
+// kernel takes it.
+template <int G>
 __global__ void __cluster_dims__(kAccCluster, 1, 1) __launch_bounds__(kAccThreads, 2)
-accept_reject_pass(AcceptKArgs a) {
+accept_reject_node(AcceptKArgs a) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ RejShared sh;
-  extern __shared__ float r_s[];     // this CTA's slice: t, then r
-  grid_dep_wait();
-  grid_dep_launch_dependents();
+  extern __shared__ float4 p_s[];   // this CTA's slice: target logits, then p
 
   const int rank = (int)cl.block_rank();
   const int node = blockIdx.x / kAccCluster;
-  const int V = a.vocab;
-  const int per = ((V + kAccCluster - 1) / kAccCluster + 3) & ~3;
-  const int v0 = min(V, rank * per), v1 = min(V, v0 + per);
-  const int n = v1 - v0;
-  const float* trow = a.tl + (int64_t)node * V + v0;
-  const float* drow = a.dl + (int64_t)node * V + v0;
+  const Slice sl = slice_of(a.vocab, rank);
+  const int n4 = sl.n4;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const bool vec = a.vec != 0;
+  const uint32_t bar = ptx::smem_addr(&sh.bar);
 
-  // ---- children of the node (warp 0, lane-parallel over candidates, in
-  // order); the other warps start on the target row meanwhile
-  if (warp == 0) {
-    const int b = seq_of(a.offsets, a.batch, node);
-    const int n0 = __ldg(a.offsets + b);
+  if (tid == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+
+  // ---- children of the node, in order (every warp counts them; warp 0
+  // also lists them).  A malformed tree (flagged by the walk) gets none, so
+  // no parent read leaves the node arrays.
+  const int b = seq_of(a.offsets, a.batch, node);
+  const int n0 = __ldg(a.offsets + b);
+  int nch = 0;
+  {
     int T = __ldg(a.offsets + b + 1) - n0;
-    // a malformed tree (flagged by the walk) gets no children, so no parent
-    // read leaves the node arrays
     if (T > DS_MAX_TREE_NODES || T < 0 || n0 < 0 || n0 + T > a.n_nodes) T = 0;
     const int i = node - n0;
-    int cnt = 0;
     for (int c0 = 0; c0 < T; c0 += 32) {
       const int c = c0 + lane;
       const bool is = c > i && c < T && __ldg(a.parents + n0 + c) == i;
       const unsigned m = __ballot_sync(0xffffffffu, is);
-      if (is) sh.children[cnt + __popc(m & ((1u << lane) - 1))] = c;
-      cnt += __popc(m);
+      if (warp == 0 && is) sh.children[nch + __popc(m & ((1u << lane) - 1))] = c;
+      nch += __popc(m);
     }
-    if (lane == 0) { sh.nch = cnt; sh.n0 = n0; }
   }
+  if (nch == 0) return;
 
-  // ---- pass 1: the target slice into shared memory; online (max, sum of
-  // exponentials) of the target, and of the draft for an inner node
-  OnlineExp ot, od;
+  // ---- the target slice into shared memory, the draft slice into registers
+  copy_target_slice(a, node, sl, p_s, bar);
+  float4 qv[G];
+  load_draft_slice<G>(a, node, sl, true, qv);
+  __syncthreads();                  // the barrier's initialisation, sh.children
+  wait_target_slice(a, sl, bar);
+
+  // ---- target and draft: max and sum of exp(l - max)
+  float Mt, Md = -CUDART_INF_F;
+  F2 St, Sd;
+  thread_online_smem<G>(p_s, n4, Mt, St);
+#pragma unroll
+  for (int j = 0; j < G; ++j) Md = fmaxf(Md, max4(qv[j]));
   {
-    const float4 ninf = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
-    if (vec) {
-      const int n4 = n >> 2;
-      const float4* t4 = reinterpret_cast<const float4*>(trow);
-      float4* r4 = reinterpret_cast<float4*>(r_s);
-      for (int base = tid; base < n4; base += 4 * kAccThreads) {
-        float4 x[4];
+    Kahan kd;
+    if (Md != -CUDART_INF_F) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = base + u * kAccThreads;
-          x[u] = e < n4 ? __ldg(t4 + e) : ninf;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = base + u * kAccThreads;
-          if (e < n4) r4[e] = x[u];
-          ot.add4(x[u]);
-        }
-      }
-    } else {
-      for (int e = tid; e < n; e += kAccThreads) {
-        const float x = __ldg(trow + e);
-        r_s[e] = x;
-        ot.add1(x);
-      }
+      for (int j = 0; j < G; ++j) kd.add(sum4(expf4(qv[j], Md)));
     }
-  }
-  __syncthreads();                  // sh.nch, sh.children
-  const int nch = sh.nch;
-  const bool inner = nch > 0;       // a leaf never reads its draft row
-  if (inner) {
-    if (vec) {
-      const int n4 = n >> 2;
-      const float4* d4 = reinterpret_cast<const float4*>(drow);
-      const float4 ninf = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
-      for (int base = tid; base < n4; base += 4 * kAccThreads) {
-        float4 x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = base + u * kAccThreads;
-          x[u] = e < n4 ? __ldg(d4 + e) : ninf;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) od.add4(x[u]);
-      }
-    } else {
-      for (int e = tid; e < n; e += kAccThreads) od.add1(__ldg(drow + e));
-    }
+    Sd = kahan_f2(kd);
   }
   int slot = 0;
-  cluster_online2(cl, sh, slot, ot.m, kahan_f2(ot.k), od.m, kahan_f2(od.k));
-  if (tid == 0) {
-    sh.fres[2] = recip_f(sh.dres[0]);
-    sh.fres[3] = inner ? recip_f(sh.dres[1]) : 0.f;
-    // a leaf draws its bonus from p, proportional to exp(t - M)
-    sh.btot = sh.dres[0]; sh.bpre = sh.dpre; sh.bmine = sh.dmine;
-  }
-  __syncthreads();
-  const float Mf = sh.fres[0], Mdf = sh.fres[1];
-  const float invSt = sh.fres[2], invSd = sh.fres[3];
-
-  // ---- residual chain, one pass per child.  The slice holds r_{k-1} (the
-  // target logits before the first pass, which forms p = exp(t - M) / S);
-  // the pass first applies the previous step (r_{k-1} = max(0, r_{k-2} - q)
-  // / Z_{k-1}) and writes it back, then adds max(0, r_{k-1} - q) into Z_k:
-  // per element the same float operations, in the same order, as the walk
-  // uses to evaluate the chain at a token.
-  float zinv_prev = 0.f;
-  for (int k = 0; k < nch; ++k) {
-    const Kahan kz = visit(drow, r_s, n, vec, true, [&](float& r, float d) {
-      const float q = expf(d - Mdf) * invSd;
-      if (k == 0) r = expf(r - Mf) * invSt;
-      else if (zinv_prev != 0.f) r = fmaxf(0.f, r - q) * zinv_prev;
-      return fmaxf(0.f, r - q);
-    });
-    cluster_sum2(cl, sh, slot, kahan_f2(kz), F2{0.f, 0.f});
-    __syncthreads();
-    if (tid == 0) {
-      sh.fres[2] = sh.dres[0] > 0.0 ? recip_f(sh.dres[0]) : 0.f;
-      if (rank == 0) a.stats[sh.n0 + sh.children[k]].zinv_after = sh.fres[2];
-      // after the last child: the bonus weights max(0, r - q) (proportional
-      // to the final residual) and their totals
-      sh.btot = sh.dres[0]; sh.bpre = sh.dpre; sh.bmine = sh.dmine;
-    }
-    __syncthreads();
-    zinv_prev = sh.fres[2];
-  }
-
-  // ---- bonus draw: the smallest x with sum_{y<=x} r_m(y) > u * sum r_m.
-  // The draw is scale-invariant, so it runs on weights proportional to r_m
-  // whose per-CTA totals the last reduction already gave: a leaf's
-  // exp(t - M) (r_m = p), an inner node's max(0, r_{m-1} - q) (r_m with
-  // Z_m > 0).  Only when Z_m = 0 (r_m = r_{m-1}, the slice itself) do the
-  // totals take one more pass.
-  int wmode = inner ? 1 : 0;        // 0: exp(t - M), 1: max(0, r - q), 2: r
-  if (inner && zinv_prev == 0.f) {
-    wmode = 2;
-    const Kahan kr = visit(drow, r_s, n, vec, false, [&](float& r, float) { return r; });
-    cluster_sum2(cl, sh, slot, kahan_f2(kr), F2{0.f, 0.f});
-    __syncthreads();
-    if (tid == 0) { sh.btot = sh.dres[0]; sh.bpre = sh.dpre; sh.bmine = sh.dmine; }
-  }
-  if (tid == 0) {
-    const double thr = (double)__ldg(a.uniforms + 2 * (int64_t)node + 1) * sh.btot;
-    const bool mine = (sh.bpre <= thr && thr < sh.bpre + sh.bmine) ||
-                      (rank == kAccCluster - 1 && thr >= sh.bpre + sh.bmine);
-    sh.fres[3] = mine ? 1.f : 0.f;
-    sh.scan[kAccWarps] = f2_of(thr - sh.bpre);   // threshold within this slice
-    sh.bonus = -1;
-  }
-  __syncthreads();
-  if (sh.fres[3] != 0.f) {
-    // rounds of 4 * kAccThreads consecutive tokens, thread t taking tokens
-    // 4t .. 4t + 3 of a round (one conflict-free 16-byte read); a block-wide
-    // scan of the round (compensated pairs) gives each thread its prefix;
-    // the first thread whose prefix passes the threshold walks its four
-    const F2 thr_rel = sh.scan[kAccWarps];
-    auto weight = [&](float r, float d) -> float {
-      if (wmode == 0) return expf(r - Mf);
-      if (wmode == 1) return fmaxf(0.f, r - expf(d - Mdf) * invSd);
-      return r;
-    };
-    auto round_vals = [&](int base, float (&v)[4]) {
-      const int e = base + 4 * tid;
-      if (vec) {
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), dv = x;
-        if (e < n) {
-          x = reinterpret_cast<const float4*>(r_s)[e >> 2];
-          if (wmode == 1) dv = __ldg(reinterpret_cast<const float4*>(drow) + (e >> 2));
-        }
-        v[0] = weight(x.x, dv.x); v[1] = weight(x.y, dv.y);
-        v[2] = weight(x.z, dv.z); v[3] = weight(x.w, dv.w);
-        if (e >= n) v[0] = v[1] = v[2] = v[3] = 0.f;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          v[q] = e + q < n ? weight(r_s[e + q], wmode == 1 ? __ldg(drow + e + q) : 0.f) : 0.f;
-      }
-    };
-    F2 running{0.f, 0.f};
-    for (int base = 0; base < n; base += 4 * kAccThreads) {
-      float v[4];
-      round_vals(base, v);
-      const F2 own = two_sum(v[0] + v[1], v[2] + v[3]);
-      F2 incl = own;
-      for (int o = 1; o < 32; o <<= 1) {
-        const F2 y = f2_shfl_up(incl, o);
-        if (lane >= o) incl = f2_add(incl, y);
-      }
-      if (lane == 31) sh.scan[warp] = incl;
-      if (tid == 0) sh.first = 0x7fffffff;
-      __syncthreads();
-      F2 wpre = running;
-      for (int w = 0; w < warp; ++w) wpre = f2_add(wpre, sh.scan[w]);
-      F2 round_tot = running;
-      for (int w = 0; w < kAccWarps; ++w) round_tot = f2_add(round_tot, sh.scan[w]);
-      const F2 incl_all = f2_add(wpre, incl);
-      if (base + 4 * tid < n && f2_gt(incl_all, thr_rel)) atomicMin(&sh.first, tid);
-      __syncthreads();
-      const int first = sh.first;
-      if (first != 0x7fffffff) {
-        if (tid == first) {
-          F2 run = f2_add(incl_all, F2{-own.hi, -own.lo});
-          int pick = min(base + 4 * tid + 3, n - 1);
-          for (int q = 0; q < 4 && base + 4 * tid + q < n; ++q) {
-            run = f2_add(run, F2{v[q], 0.f});
-            if (f2_gt(run, thr_rel)) { pick = base + 4 * tid + q; break; }
-          }
-          sh.bonus = v0 + pick;
-        }
-        break;
-      }
-      running = round_tot;
-      __syncthreads();              // sh.scan reused by the next round
-    }
-    __syncthreads();
-    if (tid == 0) {
-      // rounding left the threshold past the slice: its last token
-      a.stats[node].bonus_stop = sh.bonus >= 0 ? sh.bonus : (n > 0 ? v1 - 1 : V - 1);
-    }
-  }
+  cluster_online(cl, sh, slot, Mt, St, Md, Sd);
+  const float invSt = recip_f2(St);
+  const float invSd = recip_f2(Sd);
+  NodeStats* stats = a.stats;
   if (rank == 0 && tid == 0) {
-    a.stats[node].m_t = Mf;
-    a.stats[node].inv_s_t = invSt;
-    a.stats[node].m_d = Mdf;
-    a.stats[node].inv_s_d = invSd;
+    stats[node].m_t = Mt;
+    stats[node].inv_s_t = invSt;
+    stats[node].m_d = Md;
+    stats[node].inv_s_d = invSd;
+    stats[n0 + sh.children[0]].s_res = 0.f;      // the first child: r_0 = p
+    stats[n0 + sh.children[0]].invc_res = 1.f;
   }
-  // no CTA may exit while another can still read its shared memory
-  cl.sync();
+
+  // ---- p and q of the slice (each thread its own groups), with the first
+  // residual's sum, max(0, p - q) (s_1 = 1)
+  Kahan k1;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int e = tid + j * kAccThreads;
+    const float4 d = expf4(qv[j], Md);
+    qv[j] = make_float4(d.x * invSd, d.y * invSd, d.z * invSd, d.w * invSd);
+    if (e < n4) {
+      const float4 t = expf4(p_s[e], Mt);
+      const float4 pv = make_float4(t.x * invSt, t.y * invSt, t.z * invSt, t.w * invSt);
+      p_s[e] = pv;
+      k1.add(sum4(resid4(pv, qv[j], 1.f)));
+    }
+  }
+
+  // ---- residual chain: child k (k >= 1) is tested against r_k, the
+  // residual after its elder siblings were rejected; the last pass gives
+  // r_nch, the bonus draw's distribution if every child is rejected
+  F2 sacc{1.f, 0.f};                  // s_k = 1 + C_1 + ... + C_{k-1}
+  float s_prev = 0.f, ic_prev = 1.f;  // residual in force: r_0 = p
+  F2 part = kahan_f2(k1);
+  for (int k = 1; k <= nch; ++k) {
+    const float s = sacc.hi;
+    if (k > 1) {
+      Kahan kz;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int e = tid + j * kAccThreads;
+        if (e < n4) kz.add(sum4(resid4(p_s[e], qv[j], s)));
+      }
+      part = kahan_f2(kz);
+    }
+    const F2 C = cluster_sum(cl, sh, slot, part);
+    if (!(C.hi > 0.f)) {
+      // zero residual: r_k = r_{k-1}, and so is every later residual
+      if (rank == 0 && tid == 0)
+        for (int kk = k; kk < nch; ++kk) {
+          stats[n0 + sh.children[kk]].s_res = s_prev;
+          stats[n0 + sh.children[kk]].invc_res = ic_prev;
+        }
+      break;
+    }
+    s_prev = s;
+    ic_prev = recip_f2(C);
+    if (k < nch && rank == 0 && tid == 0) {
+      stats[n0 + sh.children[k]].s_res = s;
+      stats[n0 + sh.children[k]].invc_res = ic_prev;
+    }
+    sacc = f2_add(sacc, C);
+  }
+  if (rank == 0 && tid == 0) stats[node].s_bonus = s_prev;
+  // No CTA leaves while another can still write into its shared memory:
+  // every push happens before a cluster barrier that all CTAs pass.
 }
 
 // ---------------------------------------------------------------------------
@@ -826,33 +844,56 @@ accept_reject_pass_stream(AcceptKArgs a) {
   __syncthreads();
   const int nch = s_nch;
 
-  // ---- residual normalisers, one pass per child
-  float zinv[DS_MAX_TREE_NODES];  // only the first k entries are read
-  float zpos[DS_MAX_TREE_NODES];
-  for (int k = 0; k < nch; ++k) {
+  // ---- residual chain in closed form (see the node pass above): child k
+  // is tested against max(0, p - s_k q) / C_k, one pass per child
+  auto pq = [&](int x, float& p, float& q) {
+    p = expf(__ldg(trow + x) - M) * invSt;
+    q = expf(__ldg(drow + x) - Md) * invSd;
+  };
+  if (nch > 0 && rank == 0 && threadIdx.x == 0) {
+    a.stats[n0 + s_children[0]].s_res = 0.f;
+    a.stats[n0 + s_children[0]].invc_res = 1.f;
+  }
+  double sacc = 1.0;
+  float s_prev = 0.f, s_last = 0.f;
+  for (int k = 1; k <= nch; ++k) {
+    const float s = (float)sacc;
     Kahan kz;
     for (int x = v0 + threadIdx.x; x < v1; x += kAccThreads) {
-      const float p = expf(__ldg(trow + x) - M) * invSt;
-      const float q = expf(__ldg(drow + x) - Md) * invSd;
-      float r = p;
-      for (int j = 0; j < k; ++j)
-        if (zpos[j] > 0.f) r = fmaxf(0.f, r - q) * zinv[j];
-      kz.add(fmaxf(0.f, r - q));
+      float p, q;
+      pq(x, p, q);
+      kz.add(fmaxf(0.f, fmaf(-s, q, p)));
     }
-    const double Z = cluster_sum(cl, &cs, block_sum_d(kz.value(), s_d), 2);
-    zpos[k] = Z > 0.0 ? 1.f : 0.f;
-    zinv[k] = Z > 0.0 ? (float)(1.0 / Z) : 0.f;
-    if (rank == 0 && threadIdx.x == 0) a.stats[n0 + s_children[k]].zinv_after = zinv[k];
+    const double C = cluster_sum(cl, &cs, block_sum_d(kz.value(), s_d), 2);
+    if (C > 0.0) {
+      if (k < nch && rank == 0 && threadIdx.x == 0) {
+        a.stats[n0 + s_children[k]].s_res = s;
+        a.stats[n0 + s_children[k]].invc_res = (float)(1.0 / C);
+      }
+      sacc += C;
+      s_prev = s;
+      s_last = s;
+    } else {
+      // zero residual: r_k = r_{k-1}, and so is every later residual
+      if (rank == 0 && threadIdx.x == 0) {
+        const NodeStats prev = a.stats[n0 + s_children[k - 1]];
+        for (int kk = k; kk < nch; ++kk) {
+          a.stats[n0 + s_children[kk]].s_res = prev.s_res;
+          a.stats[n0 + s_children[kk]].invc_res = prev.invc_res;
+        }
+      }
+      s_last = s_prev;
+      break;
+    }
   }
 
-  // ---- bonus if the walk stops here: inverse CDF of r_nch
+  // ---- bonus if the walk stops here: inverse CDF of the last residual
+  // (p itself for a leaf)
   auto rval = [&](int x) -> float {
-    const float p = expf(__ldg(trow + x) - M) * invSt;
-    const float q = expf(__ldg(drow + x) - Md) * invSd;
-    float r = p;
-    for (int j = 0; j < nch; ++j)
-      if (zpos[j] > 0.f) r = fmaxf(0.f, r - q) * zinv[j];
-    return r;
+    float p, q;
+    if (nch == 0) return expf(__ldg(trow + x) - M) * invSt;
+    pq(x, p, q);
+    return fmaxf(0.f, fmaf(-s_last, q, p));
   };
   Kahan ks;
   for (int x = v0 + threadIdx.x; x < v1; x += kAccThreads) ks.add(rval(x));
@@ -959,89 +1000,236 @@ DS_DEV int greedy_argmax(const AcceptKArgs& a, int node) {
   return (int)(~(uint32_t)(k & 0xffffffffu));
 }
 
-// One warp per sequence.
-__global__ void __launch_bounds__(128) accept_walk(AcceptKArgs a) {
-  grid_dep_wait();
-  grid_dep_launch_dependents();
+// The walk of sequence b by one warp (every lane calls it): follows the tree
+// from the root and returns the stop node (global index, -1 for an empty
+// tree) and whether it has children.  With `write` it stores the path and
+// the count, and the bonus -1 of an empty tree.
+//
+// The walk reaches child c of node i only after rejecting every elder
+// sibling of c, and c's test assumes exactly that (its residual comes from
+// the node pass), so whether c would be accepted does not depend on the
+// walk: lane l evaluates the tests of nodes l and l + 32 at once, with one
+// round of loads, and the walk itself is ballots over those bits.
+struct WalkEnd {
+  int node;
+  bool inner;
+};
+DS_DEV WalkEnd walk_sequence(const AcceptKArgs& a, int b, bool write) {
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (b >= a.batch) return;
   const int n0 = __ldg(a.offsets + b), n1 = __ldg(a.offsets + b + 1);
   int T = n1 - n0;
   int32_t* path = a.out_path + (int64_t)b * DS_MAX_TREE_NODES;
-  path[lane] = -1;
-  path[lane + 32] = -1;
+  if (write) {
+    path[lane] = -1;
+    path[lane + 32] = -1;
+  }
   if (T < 0 || T > DS_MAX_TREE_NODES || n0 < 0 || n1 > a.n_nodes) {
     if (lane == 0) flag(a.status, DS_DEV_BAD_TREE);
     T = 0;
   }
   if (T == 0) {
-    if (lane == 0) { a.out_n[b] = 0; a.out_bonus[b] = -1; }
-    return;
+    if (write && lane == 0) { a.out_n[b] = 0; a.out_bonus[b] = -1; }
+    return {-1, false};
   }
   const bool reject = a.mode == DS_ACCEPT_REJECT;
   const int V = a.vocab;
-  int i = 0, n = 0;
-  for (int step = 0; step < DS_MAX_TREE_NODES; ++step) {
-    const int c0 = lane, c1 = lane + 32;
-    const bool k0 = c0 > i && c0 < T && __ldg(a.parents + n0 + c0) == i;
-    const bool k1 = c1 > i && c1 < T && __ldg(a.parents + n0 + c1) == i;
-    int next = -1;
-    if (!reject) {
-      const int y = greedy_argmax(a, n0 + i);
-      const bool m0 = k0 && __ldg(a.tokens + n0 + c0) == y;
-      const bool m1 = k1 && __ldg(a.tokens + n0 + c1) == y;
-      const unsigned b0 = __ballot_sync(0xffffffffu, m0);
-      const unsigned b1 = __ballot_sync(0xffffffffu, m1);
-      next = b0 ? __ffs(b0) - 1 : (b1 ? 32 + __ffs(b1) - 1 : -1);
-    } else {
-      const uint64_t kids = (uint64_t)__ballot_sync(0xffffffffu, k0) |
-                            ((uint64_t)__ballot_sync(0xffffffffu, k1) << 32);
-      if (lane == 0) {
-        const NodeStats st = a.stats[n0 + i];
-        uint64_t rest = kids;
-        uint64_t rejected = 0;
-        while (rest) {
-          const int c = __ffsll((long long)rest) - 1;
-          rest &= rest - 1;
-          const int x = __ldg(a.tokens + n0 + c);
-          if (x < 0 || x >= V) {
-            flag(a.status, DS_DEV_BAD_TOKEN);
-            rejected |= 1ull << c;
-            continue;
-          }
-          // p(x), q(x) and the residual after the rejected siblings, with
-          // the node pass's own float operations and scalars
-          const float p =
-              expf(__ldg(a.tl + (int64_t)(n0 + i) * V + x) - st.m_t) * st.inv_s_t;
-          const float q =
-              expf(__ldg(a.dl + (int64_t)(n0 + i) * V + x) - st.m_d) * st.inv_s_d;
-          float r = p;
-          uint64_t rj = rejected;
-          while (rj) {
-            const int cj = __ffsll((long long)rj) - 1;
-            rj &= rj - 1;
-            const float zinv = a.stats[n0 + cj].zinv_after;
-            if (zinv != 0.f) r = fmaxf(0.f, r - q) * zinv;
-          }
-          const float u = __ldg(a.uniforms + 2 * (int64_t)(n0 + c));
-          if (u * q < r) { next = c; break; }
-          rejected |= 1ull << c;
-        }
-      }
-      next = __shfl_sync(0xffffffffu, next, 0);
+  int par[2], tok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    par[h] = c < T ? __ldg(a.parents + n0 + c) : -1;
+    tok[h] = c < T ? __ldg(a.tokens + n0 + c) : 0;
+    if (!(par[h] >= 0 && par[h] < c)) par[h] = -1;   // c is a child of par[h] < c only
+  }
+  bool acc[2];
+  if (!reject) {
+    // greedy: c passes iff its token is its parent's target argmax
+    int y[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = lane + 32 * h;
+      uint64_t k = 0;
+      if (c < T)
+        for (int sl = 0; sl < a.slices; ++sl) k = u64max(k, a.stats[n0 + c].amax[sl]);
+      y[h] = (int)(~(uint32_t)(k & 0xffffffffu));
     }
-    if (next < 0) break;
-    if (lane == 0) path[n] = next;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int pp = par[h] < 0 ? 0 : par[h];
+      const int y0 = __shfl_sync(0xffffffffu, y[0], pp & 31);
+      const int y1 = __shfl_sync(0xffffffffu, y[1], pp & 31);
+      acc[h] = par[h] >= 0 && tok[h] == (pp >= 32 ? y1 : y0);
+    }
+  } else {
+    // rejection: u * q(x) < r(x) at the parent, with the node pass's own
+    // float operations and scalars; an invalid token is flagged and fails
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = lane + 32 * h;
+      acc[h] = false;
+      if (par[h] < 0) continue;
+      const int x = tok[h];
+      if (x < 0 || x >= V) {
+        flag(a.status, DS_DEV_BAD_TOKEN);
+        continue;
+      }
+      const int i = n0 + par[h];
+      const NodeStats& st = a.stats[i];
+      const float p = expf(__ldg(a.tl + (int64_t)i * V + x) - st.m_t) * st.inv_s_t;
+      const float q = expf(__ldg(a.dl + (int64_t)i * V + x) - st.m_d) * st.inv_s_d;
+      const float r = fmaxf(0.f, fmaf(-a.stats[n0 + c].s_res, q, p)) * a.stats[n0 + c].invc_res;
+      const float u = __ldg(a.uniforms + 2 * (int64_t)(n0 + c));
+      acc[h] = u * q < r;
+    }
+  }
+  int i = 0, n = 0;
+  bool inner = false;
+  for (int step = 0; step < DS_MAX_TREE_NODES; ++step) {
+    const bool k0 = par[0] == i, k1 = par[1] == i;
+    const uint64_t kids = (uint64_t)__ballot_sync(0xffffffffu, k0) |
+                          ((uint64_t)__ballot_sync(0xffffffffu, k1) << 32);
+    const uint64_t pass = (uint64_t)__ballot_sync(0xffffffffu, k0 && acc[0]) |
+                          ((uint64_t)__ballot_sync(0xffffffffu, k1 && acc[1]) << 32);
+    inner = kids != 0;
+    if (pass == 0) break;
+    const int next = __ffsll((long long)pass) - 1;   // the first child that passes
+    if (write && lane == 0) path[n] = next;
     ++n;
     i = next;
   }
-  const int bonus = reject ? a.stats[n0 + i].bonus_stop : greedy_argmax(a, n0 + i);
-  if (lane == 0) {
-    a.out_n[b] = n;
-    a.out_bonus[b] = bonus;
+  if (write && lane == 0) a.out_n[b] = n;
+  return {n0 + i, inner};
+}
+
+// One warp per sequence: greedy (bonus = the stop node's argmax) and the
+// streaming rejection pass (bonus drawn by the node pass).
+__global__ void __launch_bounds__(128) accept_walk(AcceptKArgs a) {
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (b >= a.batch) return;
+  const WalkEnd w = walk_sequence(a, b, true);
+  if (w.node < 0) return;
+  const bool reject = a.mode == DS_ACCEPT_REJECT;
+  const int bonus = reject ? a.stats[w.node].bonus_stop : greedy_argmax(a, w.node);
+  if ((threadIdx.x & 31) == 0) a.out_bonus[b] = bonus;
+}
+
+// Rejection finish: one cluster per sequence.  Warp 0 of every CTA runs the
+// same walk (CTA 0 writes the path); then the cluster draws the bonus token
+// at the stop node: the smallest x with sum_{y<=x} w(y) > u * sum_y w(y),
+// w = max(0, p - s_bonus q) after rejected children, w = exp(t - max) (that
+// is, p) at a leaf, whose normaliser this kernel computes.
+template <int G>
+__global__ void __cluster_dims__(kAccCluster, 1, 1) __launch_bounds__(kAccThreads, 2)
+accept_finish(AcceptKArgs a) {
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ RejShared sh;
+  extern __shared__ float4 p_s[];   // the stop node's target slice
+  const int rank = (int)cl.block_rank();
+  const int b = blockIdx.x / kAccCluster;
+  const Slice sl = slice_of(a.vocab, rank);
+  const int tid = threadIdx.x;
+  const uint32_t bar = ptx::smem_addr(&sh.bar);
+  if (tid == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (tid < 32) {
+    const WalkEnd w = walk_sequence(a, b, rank == 0);
+    if (tid == 0) { sh.stop = w.node; sh.inner = w.inner ? 1 : 0; }
+  }
+  __syncthreads();                  // also the barrier's initialisation
+  const int node = sh.stop;
+  if (node < 0) return;             // empty tree (uniform over the cluster)
+  const bool inner = sh.inner != 0;
+
+  copy_target_slice(a, node, sl, p_s, bar);
+  float4 wv[G];
+  load_draft_slice<G>(a, node, sl, inner, wv);
+  wait_target_slice(a, sl, bar);
+  const float u = __ldg(a.uniforms + 2 * (int64_t)node + 1);
+  int slot = 0;
+  F2 thr_rel;
+  int owner;
+  float Mt = 0.f;
+  if (inner) {
+    const NodeStats st = a.stats[node];
+    Kahan k;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int e = tid + j * kAccThreads;
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < sl.n4) {
+        const float4 t = expf4(p_s[e], st.m_t);
+        const float4 d = expf4(wv[j], st.m_d);
+        w = resid4(make_float4(t.x * st.inv_s_t, t.y * st.inv_s_t, t.z * st.inv_s_t,
+                               t.w * st.inv_s_t),
+                   make_float4(d.x * st.inv_s_d, d.y * st.inv_s_d, d.z * st.inv_s_d,
+                               d.w * st.inv_s_d),
+                   st.s_bonus);
+        k.add(sum4(w));
+      }
+      wv[j] = w;
+    }
+    cluster_sum(cl, sh, slot, kahan_f2(k));
+    owner = bonus_owner(sh, 0, false, 0.f, u, thr_rel);
+  } else {
+    F2 St, Sd{0.f, 0.f};
+    float Md = -CUDART_INF_F;
+    thread_online_smem<G>(p_s, sl.n4, Mt, St);
+    cluster_online(cl, sh, slot, Mt, St, Md, Sd);
+    owner = bonus_owner(sh, 0, true, Mt, u, thr_rel);
+  }
+  if (owner != rank) return;
+  const int x = inner
+      ? bonus_scan<G>(sh, sl.n4, thr_rel, [&](int j, int) { return wv[j]; })
+      : bonus_scan<G>(sh, sl.n4, thr_rel, [&](int, int e) { return expf4(p_s[e], Mt); });
+  if (tid == 0) a.out_bonus[b] = x >= 0 ? sl.v0 + x : a.vocab - 1;
+  // No CTA leaves while another can still write into its shared memory:
+  // every push happens before a cluster barrier that all CTAs pass.
+}
+
+template <int G>
+cudaError_t launch_reject_g(const AcceptKArgs& a, int per, cudaStream_t stream) {
+  static bool attr_set = false;   // the attribute is per device function
+  const int max_smem = G * kAccThreads * (int)sizeof(float4);
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(accept_reject_node<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(accept_finish<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               max_smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const size_t smem = (size_t)per * sizeof(float);
+  cudaError_t e = launch_dependent(accept_reject_node<G>, dim3(a.n_nodes * kAccCluster),
+                                   dim3(kAccThreads), smem, stream, a);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(accept_finish<G>, dim3(a.batch * kAccCluster), dim3(kAccThreads),
+                          smem, stream, a);
+}
+
+// Node pass and finish with G 16-byte groups of the slice per thread
+// (1 <= G <= kRejMaxG).
+cudaError_t launch_reject(int G, const AcceptKArgs& a, int per, cudaStream_t stream) {
+  switch (G) {
+    case 1: return launch_reject_g<1>(a, per, stream);
+    case 2: return launch_reject_g<2>(a, per, stream);
+    case 3: return launch_reject_g<3>(a, per, stream);
+    case 4: return launch_reject_g<4>(a, per, stream);
+    case 5: return launch_reject_g<5>(a, per, stream);
+    case 6: return launch_reject_g<6>(a, per, stream);
+    case 7: return launch_reject_g<7>(a, per, stream);
+    case 8: return launch_reject_g<8>(a, per, stream);
+    case 9: return launch_reject_g<9>(a, per, stream);
+    default: return launch_reject_g<10>(a, per, stream);
   }
 }
+static_assert(kRejMaxG == 10, "one case per G");
 
 cudaError_t launch_accept(const ds_accept_args& g, const AcceptLayout& L,
                           cudaStream_t stream) {
@@ -1067,29 +1255,18 @@ cudaError_t launch_accept(const ds_accept_args& g, const AcceptLayout& L,
   a.out_n = g.out_n_accepted;
   a.out_bonus = g.out_bonus;
   a.status = reinterpret_cast<uint32_t*>(ws);
+  const int per = ((g.vocab + kAccCluster - 1) / kAccCluster + 3) & ~3;
+  const int G = (per / 4 + kAccThreads - 1) / kAccThreads;
+  if (g.mode == DS_ACCEPT_REJECT && g.n_nodes > 0 && a.vec && G <= kRejMaxG)
+    return launch_reject(G, a, per, stream);   // node pass + finish (walk, bonus)
   cudaError_t e = cudaSuccess;
   if (g.n_nodes > 0) {
     if (g.mode != DS_ACCEPT_REJECT) {
       e = launch_dependent(accept_argmax, dim3(g.n_nodes * a.slices), dim3(kArgThreads), 0,
                            stream, a);
     } else {
-      const int per = ((g.vocab + kAccCluster - 1) / kAccCluster + 3) & ~3;
-      if (per <= kRejMaxSlice) {
-        const size_t smem = (size_t)per * sizeof(float);
-        static int attr_set = 0;   // the attribute is per device function
-        if (!attr_set) {
-          e = cudaFuncSetAttribute(accept_reject_pass,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)(kRejMaxSlice * sizeof(float)));
-          if (e != cudaSuccess) return e;
-          attr_set = 1;
-        }
-        e = launch_dependent(accept_reject_pass, dim3(g.n_nodes * kAccCluster),
-                             dim3(kAccThreads), smem, stream, a);
-      } else {
-        accept_reject_pass_stream<<<g.n_nodes * kAccCluster, kAccThreads, 0, stream>>>(a);
-        e = cudaGetLastError();
-      }
+      accept_reject_pass_stream<<<g.n_nodes * kAccCluster, kAccThreads, 0, stream>>>(a);
+      e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
   }
