@@ -229,7 +229,9 @@ struct RejShared {
   float rsum[kAccWarps][kRejMaxG];             // bonus scan: warp sums per round
   F2 rtot[kRejMaxG];                           // bonus scan: round totals
   F2 wtot[kAccWarps];                          // bonus scan: warp totals of one round
-  int32_t children[DS_MAX_TREE_NODES];
+  int32_t children[DS_MAX_TREE_NODES];         // local ids, in order
+  int32_t ctok[DS_MAX_TREE_NODES];             // their draft tokens
+  float cs[DS_MAX_TREE_NODES], cic[DS_MAX_TREE_NODES];   // their residuals (s, 1 / C)
   int32_t first, pick;
   int32_t stop, inner;                         // finish: the walk's stop node
 };
@@ -372,18 +374,15 @@ DS_DEV bool bulk_wait(uint32_t bar) {
   return true;
 }
 
-// Smallest slice index x with sum_{y <= x} w(y) > thr (slice order), w the
-// bonus weight of this node: thread t holds the 16-byte groups t + j *
-// kAccThreads, so round j is slice tokens [4 * kAccThreads * j, 4 *
-// kAccThreads * (j + 1)) in thread order.  Round totals first (warp sums,
-// then compensated sums over the warps), the round that crosses the
-// threshold next, then a block scan of that round.  When rounding leaves the
-// threshold past everything, the last token of positive weight.  Owner CTA
-// only; returns the slice index (or -1 for an empty slice).
+// Bonus draw within one CTA's slice.  w is the node's bonus weight; thread t
+// holds the 16-byte groups t + j * kAccThreads, so round j is slice tokens
+// [4 * kAccThreads * j, 4 * kAccThreads * (j + 1)) in thread order.
+//
+// round_totals: sh.rtot[j] = compensated total of round j (warp sums, then
+// pairs over the warps); returns their sum in round order, the CTA's total.
 template <int G, class W>
-DS_DEV int bonus_scan(RejShared& sh, int n4, F2 thr_rel, W weight) {
+DS_DEV F2 round_totals(RejShared& sh, int n4, W weight) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // ---- round totals
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const int e = tid + j * kAccThreads;
@@ -405,6 +404,20 @@ DS_DEV int bonus_scan(RejShared& sh, int n4, F2 thr_rel, W weight) {
     if (lane == 0) sh.rtot[warp] = y;
   }
   __syncthreads();
+  F2 tot{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < G; ++j) tot = f2_add(tot, sh.rtot[j]);
+  return tot;
+}
+
+// scan_round (after round_totals): the smallest slice index x with
+// sum_{y <= x} w(y) > thr_rel: the round whose running total crosses the
+// threshold, then a block scan of that round.  When rounding leaves the
+// threshold past everything, the last token of positive weight.  Returns
+// the slice index (or -1 for an empty slice).
+template <int G, class W>
+DS_DEV int scan_round(RejShared& sh, int n4, F2 thr_rel, W weight) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // ---- the round that crosses (every thread, the same arithmetic)
   int js = -1, jlast = -1;
   F2 base{0.f, 0.f};
@@ -470,6 +483,15 @@ DS_DEV int bonus_scan(RejShared& sh, int n4, F2 thr_rel, W weight) {
   }
   __syncthreads();
   return sh.pick;
+}
+
+// Every CTA pushes one value (the same in all its threads) into every CTA's
+// sh.part[slot][rank]; one cluster barrier.
+DS_DEV void cluster_push(cg::cluster_group& cl, RejShared& sh, int& slot, F2 v) {
+  if (threadIdx.x < kAccCluster)
+    *cl.map_shared_rank(&sh.part[slot][cl.block_rank()][0], threadIdx.x) = v;
+  cl.sync();
+  slot ^= 1;
 }
 
 DS_DEV float4 expf4(float4 x, float m) {
@@ -594,7 +616,11 @@ accept_reject_node(AcceptKArgs a) {
       const int c = c0 + lane;
       const bool is = c > i && c < T && __ldg(a.parents + n0 + c) == i;
       const unsigned m = __ballot_sync(0xffffffffu, is);
-      if (warp == 0 && is) sh.children[nch + __popc(m & ((1u << lane) - 1))] = c;
+      if (warp == 0 && is) {
+        const int k = nch + __popc(m & ((1u << lane) - 1));
+        sh.children[k] = c;
+        sh.ctok[k] = __ldg(a.tokens + n0 + c);
+      }
       nch += __popc(m);
     }
   }
@@ -607,20 +633,33 @@ accept_reject_node(AcceptKArgs a) {
   __syncthreads();                  // the barrier's initialisation, sh.children
   wait_target_slice(a, sl, bar);
 
-  // ---- target and draft: max and sum of exp(l - max)
-  float Mt, Md = -CUDART_INF_F;
+  // ---- target and draft: per thread, max m and exp(l - m), kept (target in
+  // shared memory, draft in registers) with their compensated sums
+  float mt = -CUDART_INF_F, md = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int e = tid + j * kAccThreads;
+    if (e < n4) mt = fmaxf(mt, max4(p_s[e]));
+    md = fmaxf(md, max4(qv[j]));
+  }
   F2 St, Sd;
-  thread_online_smem<G>(p_s, n4, Mt, St);
-#pragma unroll
-  for (int j = 0; j < G; ++j) Md = fmaxf(Md, max4(qv[j]));
   {
-    Kahan kd;
-    if (Md != -CUDART_INF_F) {
+    Kahan kt, kd;
 #pragma unroll
-      for (int j = 0; j < G; ++j) kd.add(sum4(expf4(qv[j], Md)));
+    for (int j = 0; j < G; ++j) {
+      const int e = tid + j * kAccThreads;
+      if (e < n4) {
+        const float4 x = mt == -CUDART_INF_F ? make_float4(0.f, 0.f, 0.f, 0.f) : expf4(p_s[e], mt);
+        p_s[e] = x;
+        kt.add(sum4(x));
+      }
+      qv[j] = md == -CUDART_INF_F ? make_float4(0.f, 0.f, 0.f, 0.f) : expf4(qv[j], md);
+      kd.add(sum4(qv[j]));
     }
+    St = kahan_f2(kt);
     Sd = kahan_f2(kd);
   }
+  float Mt = mt, Md = md;
   int slot = 0;
   cluster_online(cl, sh, slot, Mt, St, Md, Sd);
   const float invSt = recip_f2(St);
@@ -631,21 +670,25 @@ accept_reject_node(AcceptKArgs a) {
     stats[node].inv_s_t = invSt;
     stats[node].m_d = Md;
     stats[node].inv_s_d = invSd;
-    stats[n0 + sh.children[0]].s_res = 0.f;      // the first child: r_0 = p
-    stats[n0 + sh.children[0]].invc_res = 1.f;
+  }
+  if (tid == 0) {
+    sh.cs[0] = 0.f;                  // the first child: r_0 = p
+    sh.cic[0] = 1.f;
   }
 
-  // ---- p and q of the slice (each thread its own groups), with the first
-  // residual's sum, max(0, p - q) (s_1 = 1)
+  // ---- p = exp(t - m) * (exp(m - M) / S) and q likewise (each thread its
+  // own groups), with the first residual's sum, max(0, p - q) (s_1 = 1)
+  const float ft = mt == -CUDART_INF_F ? 0.f : expf(mt - Mt) * invSt;
+  const float fd = md == -CUDART_INF_F ? 0.f : expf(md - Md) * invSd;
   Kahan k1;
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const int e = tid + j * kAccThreads;
-    const float4 d = expf4(qv[j], Md);
-    qv[j] = make_float4(d.x * invSd, d.y * invSd, d.z * invSd, d.w * invSd);
+    const float4 d = qv[j];
+    qv[j] = make_float4(d.x * fd, d.y * fd, d.z * fd, d.w * fd);
     if (e < n4) {
-      const float4 t = expf4(p_s[e], Mt);
-      const float4 pv = make_float4(t.x * invSt, t.y * invSt, t.z * invSt, t.w * invSt);
+      const float4 t = p_s[e];
+      const float4 pv = make_float4(t.x * ft, t.y * ft, t.z * ft, t.w * ft);
       p_s[e] = pv;
       k1.add(sum4(resid4(pv, qv[j], 1.f)));
     }
@@ -671,22 +714,37 @@ accept_reject_node(AcceptKArgs a) {
     const F2 C = cluster_sum(cl, sh, slot, part);
     if (!(C.hi > 0.f)) {
       // zero residual: r_k = r_{k-1}, and so is every later residual
-      if (rank == 0 && tid == 0)
-        for (int kk = k; kk < nch; ++kk) {
-          stats[n0 + sh.children[kk]].s_res = s_prev;
-          stats[n0 + sh.children[kk]].invc_res = ic_prev;
-        }
+      if (tid == 0)
+        for (int kk = k; kk < nch; ++kk) { sh.cs[kk] = s_prev; sh.cic[kk] = ic_prev; }
       break;
     }
     s_prev = s;
     ic_prev = recip_f2(C);
-    if (k < nch && rank == 0 && tid == 0) {
-      stats[n0 + sh.children[k]].s_res = s;
-      stats[n0 + sh.children[k]].invc_res = ic_prev;
-    }
+    if (k < nch && tid == 0) { sh.cs[k] = s; sh.cic[k] = ic_prev; }
     sacc = f2_add(sacc, C);
   }
   if (rank == 0 && tid == 0) stats[node].s_bonus = s_prev;
+
+  // ---- each child's test u * q(x) < r(x), by the thread that holds its
+  // token x: p(x) and q(x) are that thread's own values, so the walk needs
+  // only the outcome (tokens outside the vocabulary are the walk's to flag)
+  __syncthreads();                  // sh.cs, sh.cic
+  for (int k = 0; k < nch; ++k) {
+    const int g = sh.ctok[k] - sl.v0;
+    if (g < 0 || g >= 4 * n4 || ((g >> 2) & (kAccThreads - 1)) != tid) continue;
+    const int jj = (g >> 2) / kAccThreads;
+    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+      if (j == jj) q4 = qv[j];
+    const float4 p4 = p_s[g >> 2];
+    const int c3 = g & 3;
+    const float q = c3 == 0 ? q4.x : c3 == 1 ? q4.y : c3 == 2 ? q4.z : q4.w;
+    const float pv = c3 == 0 ? p4.x : c3 == 1 ? p4.y : c3 == 2 ? p4.z : p4.w;
+    const float r = fmaxf(0.f, fmaf(-sh.cs[k], q, pv)) * sh.cic[k];
+    const int c = n0 + sh.children[k];
+    stats[c].pass = __ldg(a.uniforms + 2 * (int64_t)c) * q < r ? 1 : 0;
+  }
   // No CTA leaves while another can still write into its shared memory:
   // every push happens before a cluster barrier that all CTAs pass.
 }
@@ -850,10 +908,8 @@ accept_reject_pass_stream(AcceptKArgs a) {
     p = expf(__ldg(trow + x) - M) * invSt;
     q = expf(__ldg(drow + x) - Md) * invSd;
   };
-  if (nch > 0 && rank == 0 && threadIdx.x == 0) {
-    a.stats[n0 + s_children[0]].s_res = 0.f;
-    a.stats[n0 + s_children[0]].invc_res = 1.f;
-  }
+  __shared__ float s_cs[DS_MAX_TREE_NODES], s_cic[DS_MAX_TREE_NODES];
+  if (threadIdx.x == 0) { s_cs[0] = 0.f; s_cic[0] = 1.f; }
   double sacc = 1.0;
   float s_prev = 0.f, s_last = 0.f;
   for (int k = 1; k <= nch; ++k) {
@@ -866,24 +922,30 @@ accept_reject_pass_stream(AcceptKArgs a) {
     }
     const double C = cluster_sum(cl, &cs, block_sum_d(kz.value(), s_d), 2);
     if (C > 0.0) {
-      if (k < nch && rank == 0 && threadIdx.x == 0) {
-        a.stats[n0 + s_children[k]].s_res = s;
-        a.stats[n0 + s_children[k]].invc_res = (float)(1.0 / C);
-      }
+      if (k < nch && threadIdx.x == 0) { s_cs[k] = s; s_cic[k] = (float)(1.0 / C); }
       sacc += C;
       s_prev = s;
       s_last = s;
     } else {
       // zero residual: r_k = r_{k-1}, and so is every later residual
-      if (rank == 0 && threadIdx.x == 0) {
-        const NodeStats prev = a.stats[n0 + s_children[k - 1]];
-        for (int kk = k; kk < nch; ++kk) {
-          a.stats[n0 + s_children[kk]].s_res = prev.s_res;
-          a.stats[n0 + s_children[kk]].invc_res = prev.invc_res;
-        }
-      }
+      if (threadIdx.x == 0)
+        for (int kk = k; kk < nch; ++kk) { s_cs[kk] = s_cs[k - 1]; s_cic[kk] = s_cic[k - 1]; }
       s_last = s_prev;
       break;
+    }
+  }
+
+  // ---- each child's test at its token (rank 0, one thread per child)
+  __syncthreads();
+  if (rank == 0 && (int)threadIdx.x < nch) {
+    const int k = threadIdx.x;
+    const int c = n0 + s_children[k];
+    const int x = __ldg(a.tokens + c);
+    if (x >= 0 && x < V) {
+      float p, q;
+      pq(x, p, q);
+      const float r = fmaxf(0.f, fmaf(-s_cs[k], q, p)) * s_cic[k];
+      a.stats[c].pass = __ldg(a.uniforms + 2 * (int64_t)c) * q < r ? 1 : 0;
     }
   }
 
@@ -1006,10 +1068,10 @@ DS_DEV int greedy_argmax(const AcceptKArgs& a, int node) {
 // the count, and the bonus -1 of an empty tree.
 //
 // The walk reaches child c of node i only after rejecting every elder
-// sibling of c, and c's test assumes exactly that (its residual comes from
-// the node pass), so whether c would be accepted does not depend on the
-// walk: lane l evaluates the tests of nodes l and l + 32 at once, with one
-// round of loads, and the walk itself is ballots over those bits.
+// sibling of c, and c's test assumes exactly that, so whether c would be
+// accepted does not depend on the walk: greedy compares c's token with its
+// parent's argmax, rejection reads the outcome the node pass computed; lane
+// l holds nodes l and l + 32, and the walk itself is ballots over those bits.
 struct WalkEnd {
   int node;
   bool inner;
@@ -1061,25 +1123,18 @@ DS_DEV WalkEnd walk_sequence(const AcceptKArgs& a, int b, bool write) {
       acc[h] = par[h] >= 0 && tok[h] == (pp >= 32 ? y1 : y0);
     }
   } else {
-    // rejection: u * q(x) < r(x) at the parent, with the node pass's own
-    // float operations and scalars; an invalid token is flagged and fails
+    // rejection: the node pass evaluated each child's test u * q(x) < r(x)
+    // at its parent; an invalid token is flagged here and fails
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int c = lane + 32 * h;
       acc[h] = false;
       if (par[h] < 0) continue;
-      const int x = tok[h];
-      if (x < 0 || x >= V) {
+      if (tok[h] < 0 || tok[h] >= V) {
         flag(a.status, DS_DEV_BAD_TOKEN);
         continue;
       }
-      const int i = n0 + par[h];
-      const NodeStats& st = a.stats[i];
-      const float p = expf(__ldg(a.tl + (int64_t)i * V + x) - st.m_t) * st.inv_s_t;
-      const float q = expf(__ldg(a.dl + (int64_t)i * V + x) - st.m_d) * st.inv_s_d;
-      const float r = fmaxf(0.f, fmaf(-a.stats[n0 + c].s_res, q, p)) * a.stats[n0 + c].invc_res;
-      const float u = __ldg(a.uniforms + 2 * (int64_t)(n0 + c));
-      acc[h] = u * q < r;
+      acc[h] = a.stats[n0 + c].pass != 0;
     }
   }
   int i = 0, n = 0;
@@ -1157,7 +1212,6 @@ accept_finish(AcceptKArgs a) {
   float Mt = 0.f;
   if (inner) {
     const NodeStats st = a.stats[node];
-    Kahan k;
 #pragma unroll
     for (int j = 0; j < G; ++j) {
       const int e = tid + j * kAccThreads;
@@ -1170,12 +1224,18 @@ accept_finish(AcceptKArgs a) {
                    make_float4(d.x * st.inv_s_d, d.y * st.inv_s_d, d.z * st.inv_s_d,
                                d.w * st.inv_s_d),
                    st.s_bonus);
-        k.add(sum4(w));
       }
       wv[j] = w;
     }
-    cluster_sum(cl, sh, slot, kahan_f2(k));
+    // every CTA's round totals; the CTA partials are their sums, so the
+    // owner's scan sees exactly the totals the ownership was decided on
+    const F2 mine = round_totals<G>(sh, sl.n4, [&](int j, int) { return wv[j]; });
+    cluster_push(cl, sh, slot, mine);
     owner = bonus_owner(sh, 0, false, 0.f, u, thr_rel);
+    if (owner != rank) return;
+    const int x = scan_round<G>(sh, sl.n4, thr_rel, [&](int j, int) { return wv[j]; });
+    if (tid == 0) a.out_bonus[b] = x >= 0 ? sl.v0 + x : a.vocab - 1;
+    return;
   } else {
     F2 St, Sd{0.f, 0.f};
     float Md = -CUDART_INF_F;
@@ -1184,9 +1244,9 @@ accept_finish(AcceptKArgs a) {
     owner = bonus_owner(sh, 0, true, Mt, u, thr_rel);
   }
   if (owner != rank) return;
-  const int x = inner
-      ? bonus_scan<G>(sh, sl.n4, thr_rel, [&](int j, int) { return wv[j]; })
-      : bonus_scan<G>(sh, sl.n4, thr_rel, [&](int, int e) { return expf4(p_s[e], Mt); });
+  auto leaf_w = [&](int, int e) { return expf4(p_s[e], Mt); };
+  round_totals<G>(sh, sl.n4, leaf_w);
+  const int x = scan_round<G>(sh, sl.n4, thr_rel, leaf_w);
   if (tid == 0) a.out_bonus[b] = x >= 0 ? sl.v0 + x : a.vocab - 1;
   // No CTA leaves while another can still write into its shared memory:
   // every push happens before a cluster barrier that all CTAs pass.

@@ -57,14 +57,14 @@ inline int accept_argmax_slices(int vocab) {
 struct NodeStats {
   float m_t, inv_s_t;   // target: max logit, 1 / sum exp(l - max)   (rejection)
   float m_d, inv_s_d;   // draft:  the same                          (rejection)
-  // residual this node is tested against as a child, given that its elder
-  // siblings were rejected: r(x) = max(0, p(x) - s_res q(x)) * invc_res with
-  // p, q its parent's distributions (s_res = 0, invc_res = 1: r = p)  (rejection)
-  float s_res, invc_res;
   // bonus distribution if the walk stops here after rejecting every child:
   // proportional to max(0, p - s_bonus q)          (rejection, inner node)
   float s_bonus;
   int32_t bonus_stop;   // bonus token if the walk stops here  (streaming pass)
+  // 1 when this node, as a child, passes its test u * q(x) < r(x) at its
+  // parent, r the residual after its elder siblings were rejected (rejection)
+  int32_t pass;
+  int32_t pad_;
   uint64_t amax[kArgmaxSlices];   // greedy: per slice, the largest key
                                   // (order-preserving bits of the logit << 32
                                   // | ~index), so the maximum key is the
