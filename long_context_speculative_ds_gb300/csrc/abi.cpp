@@ -108,6 +108,8 @@ VerifyLayout verify_layout(const ds_verify_args& a, int num_sms) {
   size_t off = kStatusBytes;
   L.counters = off;
   off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * sizeof(uint32_t));
+  L.gdesc = off;
+  off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * sizeof(int32_t) * 4);
   L.o_part = off;
   off = align_up(off + (size_t)L.max_items * kRowsPerItem * a.head_dim * sizeof(float));
   L.lse_part = off;

@@ -36,35 +36,34 @@ namespace ds {
 // group formed.
 //
 // combine (the first n_comb CTAs): one warp per (sequence, kv head, row
-//   group, row).  The outputs of the row's first kCombBatch splits
-//   (lane-parallel over columns), the split log2-sum-exps (lane-parallel
-//   over splits) and the row's final log2-sum-exp are loaded in one round
-//   trip; the weights 2^{lse_s - lse} are broadcast from the lane that holds
-//   split s.
+//   group, row).  The sequence's sizes and the row group's descriptor (its
+//   first split item and split count, written by its last split) come in one
+//   round trip; then the outputs of kCombBatch splits at a time (lane-
+//   parallel over columns) together with their log2-sum-exps (lane-parallel
+//   over splits) and the row's final log2-sum-exp; the weights 2^{lse_s -
+//   lse} are broadcast from the lane that holds split s.  The batch keeps the
+//   kernel within 64 registers, so that every CTA of the launch is resident
+//   at once.
 // finalize (the rest): one warp per (chunk, sequence).  Lane i covers rows
 //   4i .. 4i + 3 and 128 + 4i .. 128 + 4i + 3 of every (kv head, row group)
-//   with 16-byte loads; four (kv head, row group) combinations per round.
-constexpr int kCombBatch = 24;
+//   with 16-byte loads; kFinCombos (kv head, row group) combinations per
+//   round.
+constexpr int kCombBatch = 8;
+constexpr int kFinCombos = 3;   // (kv head, row group) combinations per finalize round
 constexpr int kFinishThreads = 256;
 constexpr int kFinishWarps = kFinishThreads / 32;
 
 template <int D>
 DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
-  __shared__ Plan s_plan;
   const int row_blocks = kRowsPerGroup / kFinishWarps;
   const int grp = blk / row_blocks, rblk = blk % row_blocks;
   const int per_b = a.plan.num_kv_heads * a.plan.rg_max;
   const int b = grp / per_b;
   const int h = (grp / a.plan.rg_max) % a.plan.num_kv_heads;
   const int rgi = grp % a.plan.rg_max;
-  if (threadIdx.x < 32) {
-    Plan p = plan_find(a.plan, b, 0);
-    if (threadIdx.x == 0) s_plan = p;
-  }
-  __syncthreads();
-  const Plan p = s_plan;
-  const SeqPlan& sq = p.seq;
-  if (p.b < 0 || rgi >= sq.rg) return;
+  const SeqPlan sq = seq_sizes(a.plan, b, false);
+  const int4 gd = __ldcg(a.gdesc + grp);
+  if (sq.T == 0 || rgi >= sq.rg) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = rblk * kFinishWarps + warp;
   const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
@@ -73,60 +72,42 @@ DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   const int grow = rgi * kRowsPerGroup + r;
   const int node = sq.node0 + grow / G;
   const int qh = h * G + grow % G;
-  const int base = sq.item_base + (h * sq.rg + rgi) * sq.splits;
-  const int ns = sq.splits;
+  const int base = gd.x;
+  const int ns = gd.y;
   const float* lp = a.lse_part + (int64_t)base * kRowsPerGroup + r;
   constexpr int E = D / 32;   // floats per lane (4 or 2)
   const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
   const int64_t sstride = (int64_t)kRowsPerGroup * D;
+  const float lse = __ldcg(a.row_lse + (int64_t)grp * kRowsPerGroup + r);
 
-  auto load_o = [&](int s, float (&x)[E]) {
-    const float* op = op0 + (int64_t)s * sstride;
-    if constexpr (E == 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(op));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    } else {
-      const float2 v = __ldg(reinterpret_cast<const float2*>(op));
-      x[0] = v.x; x[1] = v.y;
-    }
-  };
-  float x[kCombBatch][E];
-#pragma unroll
-  for (int k = 0; k < kCombBatch; ++k) {
-    if (k < ns) load_o(k, x[k]);
-  }
-  const float l0 = lane < ns ? __ldg(lp + (int64_t)lane * kRowsPerGroup) : -CUDART_INF_F;
-  const float lse = __ldg(a.row_lse + ((((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max +
-                                        rgi) * kRowsPerGroup + r));
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  // weight of split `lane` (of the first 32), broadcast below
-  const float w0 = lane < ns ? exp2f(l0 - lse) : 0.f;
+  for (int s0 = 0; s0 < ns; s0 += kCombBatch) {
+    float x[kCombBatch][E];
 #pragma unroll
-  for (int k = 0; k < kCombBatch; ++k) {
-    const float w = __shfl_sync(0xffffffffu, w0, k);
-    if (k < ns && w != 0.f) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
+    for (int k = 0; k < kCombBatch; ++k) {
+      if (s0 + k < ns) {
+        const float* op = op0 + (int64_t)(s0 + k) * sstride;
+        if constexpr (E == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(op));
+          x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(op));
+          x[k][0] = v.x; x[k][1] = v.y;
+        }
+      }
     }
-  }
-  // more than kCombBatch splits: the rest eight at a time
-  for (int s0 = kCombBatch; s0 < ns; s0 += 8) {
-    float y[8][E];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (s0 + k < ns) load_o(s0 + k, y[k]);
-    }
-    const float wl = (s0 + (lane & 7) < ns)
-                         ? exp2f(__ldg(lp + (int64_t)(s0 + (lane & 7)) * kRowsPerGroup) - lse)
+    // weight of split s0 + lane (lanes below kCombBatch), broadcast below
+    const float wl = (lane < kCombBatch && s0 + lane < ns)
+                         ? exp2f(__ldcg(lp + (int64_t)(s0 + lane) * kRowsPerGroup) - lse)
                          : 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kCombBatch; ++k) {
       const float w = __shfl_sync(0xffffffffu, wl, k);
       if (s0 + k < ns && w != 0.f) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, y[k][e], acc[e]);
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
       }
     }
   }
@@ -154,10 +135,10 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
   static_assert(kRowsPerGroup == 256, "two 128-row halves of four rows per lane");
   float sum = 0.f;
   const int combos = a.plan.num_kv_heads * sq.rg;
-  for (int cb0 = 0; cb0 < combos; cb0 += 4) {
-    float4 v[4][2], w[4][2];
+  for (int cb0 = 0; cb0 < combos; cb0 += kFinCombos) {
+    float4 v[kFinCombos][2], w[kFinCombos][2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kFinCombos; ++k) {
       const int cb = cb0 + k;
       if (cb < combos) {
         const int h = cb / sq.rg, rgi = cb % sq.rg;
@@ -173,7 +154,7 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kFinCombos; ++k) {
       const int cb = cb0 + k;
       if (cb < combos) {
         const int rows_here = min(kRowsPerGroup, sq.rows - (cb % sq.rg) * kRowsPerGroup);
@@ -197,7 +178,7 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kFinishThreads) verify_finish(VerifyKArgs a, int n_comb) {
+__global__ void __launch_bounds__(kFinishThreads, 4) verify_finish(VerifyKArgs a, int n_comb) {
   grid_dep_wait();
   grid_dep_launch_dependents();
   if ((int)blockIdx.x < n_comb) combine_row<D>(a, blockIdx.x);
@@ -258,6 +239,7 @@ cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
   const float scale = a.scale != 0.f ? a.scale : 1.0f / sqrtf((float)a.head_dim);
   k.scale_log2 = scale * kLog2e;
   k.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  k.gdesc = reinterpret_cast<int4*>(ws + L.gdesc);
   k.o_part = reinterpret_cast<float*>(ws + L.o_part);
   k.lse_part = reinterpret_cast<float*>(ws + L.lse_part);
   k.clse = reinterpret_cast<float*>(ws + L.clse);

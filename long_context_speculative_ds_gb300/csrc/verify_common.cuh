@@ -19,6 +19,7 @@ struct VerifyKArgs {
   int64_t page_stride, tok_stride, head_stride;   // elements
   float scale_log2;
   uint32_t* counters;
+  int4* gdesc;
   float* o_part;
   float* lse_part;
   float* clse;

@@ -857,36 +857,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 5; ++i) diag[2 + i] = ctrl->where[i];
   }
   // The last split of a (sequence, kv head, row group) to finish forms the
-  // rows' final log2-sum-exp from every split's, so that the finish kernel
-  // can merge outputs and normalise chunk masses independently.  Every split
-  // counts (a timed-out one too), and the last resets the counter to zero
-  // for the next call.
+  // rows' final log2-sum-exp from every split's, and records where the row
+  // group's splits are, so that the finish kernel can merge outputs and
+  // normalise chunk masses independently.  Every split counts (a timed-out
+  // one too), and the last resets the counter to zero for the next call.
   if (active && nt > 0) {
     const int64_t cidx = ((int64_t)p.b * a.plan.num_kv_heads + kvh) * a.plan.rg_max + rgi;
+    const int64_t base = (int64_t)sq.item_base + (kvh * sq.rg + rgi) * sq.splits;
     if (threadIdx.x == 0) {
       __threadfence();            // this split's outputs before its arrival
       const uint32_t prev = atomicAdd(a.counters + cidx, 1u);
       const int last = prev + 1 == (uint32_t)sq.splits;
       if (last) {
         a.counters[cidx] = 0u;
+        a.gdesc[cidx] = make_int4((int)base, sq.splits, 0, 0);
         __threadfence();          // the other splits' outputs before reading them
       }
       ctrl->last = last;
     }
     __syncthreads();
     if (ctrl->last) {
-      const int64_t base = (int64_t)sq.item_base + (kvh * sq.rg + rgi) * sq.splits;
+      // one row per thread; the splits' values sixteen loads at a time,
+      // merged as a running (max, sum of 2^(x - max))
+      constexpr int kB = 16;
       for (int r = threadIdx.x; r < rows_here; r += kThreads) {
         const float* lp = a.lse_part + base * kRowsPerGroup + r;
-        float mx = -CUDART_INF_F;
-        for (int sp = 0; sp < sq.splits; ++sp)
-          mx = fmaxf(mx, __ldcg(lp + (int64_t)sp * kRowsPerGroup));
-        float sum = 0.f;
-        if (mx != -CUDART_INF_F)
-          for (int sp = 0; sp < sq.splits; ++sp)
-            sum += exp2f(__ldcg(lp + (int64_t)sp * kRowsPerGroup) - mx);
-        a.row_lse[cidx * kRowsPerGroup + r] =
-            sum > 0.f ? mx + log2f(sum) : -CUDART_INF_F;
+        float mx = -CUDART_INF_F, sum = 0.f;
+        for (int s0 = 0; s0 < sq.splits; s0 += kB) {
+          float v[kB];
+#pragma unroll
+          for (int k = 0; k < kB; ++k)
+            v[k] = s0 + k < sq.splits ? __ldcg(lp + (int64_t)(s0 + k) * kRowsPerGroup)
+                                      : -CUDART_INF_F;
+          float bm = v[0];
+#pragma unroll
+          for (int k = 1; k < kB; ++k) bm = fmaxf(bm, v[k]);
+          const float nm = fmaxf(mx, bm);
+          if (nm == -CUDART_INF_F) continue;
+          float add = 0.f;
+#pragma unroll
+          for (int k = 0; k < kB; ++k) add += exp2f(v[k] - nm);
+          sum = (mx == -CUDART_INF_F ? 0.f : sum * exp2f(mx - nm)) + add;
+          mx = nm;
+        }
+        a.row_lse[cidx * kRowsPerGroup + r] = sum > 0.f ? mx + log2f(sum) : -CUDART_INF_F;
       }
     }
   }
