@@ -61,11 +61,13 @@ DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   const int b = grp / per_b;
   const int h = (grp / a.plan.rg_max) % a.plan.num_kv_heads;
   const int rgi = grp % a.plan.rg_max;
-  const SeqPlan sq = seq_sizes(a.plan, b, false);
-  const int4 gd = __ldcg(a.gdesc + grp);
-  if (sq.T == 0 || rgi >= sq.rg) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = rblk * kFinishWarps + warp;
+  // sizes, descriptor and the row's final log2-sum-exp in one round trip
+  const SeqPlan sq = seq_sizes(a.plan, b, false);
+  const int4 gd = __ldcg(a.gdesc + grp);
+  const float lse = __ldcg(a.row_lse + (int64_t)grp * kRowsPerGroup + r);
+  if (sq.T == 0 || rgi >= sq.rg) return;
   const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
   if (r >= rows_here) return;
   const int G = a.plan.group;
@@ -78,7 +80,6 @@ DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   constexpr int E = D / 32;   // floats per lane (4 or 2)
   const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
   const int64_t sstride = (int64_t)kRowsPerGroup * D;
-  const float lse = __ldcg(a.row_lse + (int64_t)grp * kRowsPerGroup + r);
 
   float acc[E];
 #pragma unroll
@@ -129,35 +130,43 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
   const int b = blk / nblk_b;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = (blk % nblk_b) * kFinishWarps + warp;
-  const SeqPlan sq = seq_sizes(a.plan, b, false);
-  const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
-  if (c >= n_ch) return;
+  if (c >= a.plan.max_chunks) return;
   static_assert(kRowsPerGroup == 256, "two 128-row halves of four rows per lane");
-  float sum = 0.f;
-  const int combos = a.plan.num_kv_heads * sq.rg;
-  for (int cb0 = 0; cb0 < combos; cb0 += kFinCombos) {
-    float4 v[kFinCombos][2], w[kFinCombos][2];
+  // Combinations are enumerated over the workspace's fixed (kv head, row
+  // group) layout, so the first round's loads are issued together with the
+  // sequence's sizes; combinations and rows the sequence does not have are
+  // masked once the sizes are known.
+  const int rg_max = a.plan.rg_max;
+  const int combos = a.plan.num_kv_heads * rg_max;
+  float4 v[kFinCombos][2], w[kFinCombos][2];
+  auto load = [&](int cb0) {
 #pragma unroll
     for (int k = 0; k < kFinCombos; ++k) {
-      const int cb = cb0 + k;
-      if (cb < combos) {
-        const int h = cb / sq.rg, rgi = cb % sq.rg;
-        const int64_t hb = ((int64_t)b * a.plan.num_kv_heads + h) * a.plan.rg_max + rgi;
+      if (cb0 + k < combos) {
+        const int64_t hb = (int64_t)b * combos + cb0 + k;
         const float4* cl = reinterpret_cast<const float4*>(
             a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup);
         const float4* rl = reinterpret_cast<const float4*>(a.row_lse + hb * kRowsPerGroup);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          v[k][q] = __ldg(cl + lane + 32 * q);
+          v[k][q] = __ldcg(cl + lane + 32 * q);
           w[k][q] = __ldg(rl + lane + 32 * q);
         }
       }
     }
+  };
+  load(0);
+  const SeqPlan sq = seq_sizes(a.plan, b, false);
+  const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
+  if (c >= n_ch) return;
+  float sum = 0.f;
+  for (int cb0 = 0; cb0 < combos; cb0 += kFinCombos) {
+    if (cb0 > 0) load(cb0);
 #pragma unroll
     for (int k = 0; k < kFinCombos; ++k) {
-      const int cb = cb0 + k;
-      if (cb < combos) {
-        const int rows_here = min(kRowsPerGroup, sq.rows - (cb % sq.rg) * kRowsPerGroup);
+      const int rgi = (cb0 + k) % rg_max;
+      if (cb0 + k < combos && rgi < sq.rg) {
+        const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int r0 = 4 * lane + 128 * q;
