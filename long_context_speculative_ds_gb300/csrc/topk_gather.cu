@@ -18,6 +18,7 @@
 
 #include "dev_common.cuh"
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace ds {
 
@@ -95,11 +96,19 @@ void set_rope_turns(GatherKArgs& a, float base, int head_dim) {
   }
 }
 
+// Candidate keys held in registers: kSelRegs per thread, so up to
+// kSelRegs * kSelThreads candidates are read from memory once; candidates
+// beyond that (contexts above 16K chunks) are re-read in every round.
+constexpr int kSelRegs = 4;
+
 __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
   __shared__ uint32_t hist[256];
   __shared__ int s_warp[33];
-  __shared__ uint32_t s_prefix, s_krem, s_lt;
+  __shared__ uint32_t s_prefix, s_krem;
+  grid_dep_wait();                  // the scores come from the preceding kernels
+  grid_dep_launch_dependents();
   const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
   int L = __ldg(a.ctx_lens + b);
   if (L < 0 || (int64_t)L > (int64_t)a.max_pages * a.page_size ||
       (L + a.chunk_size - 1) / a.chunk_size > a.max_chunks) {
@@ -112,23 +121,40 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
   const float* sc = a.scores + (int64_t)b * a.max_chunks;
   int32_t* ids = a.out_chunk_ids + (int64_t)b * a.top_k;
 
-  uint32_t prefix = 0, krem = (uint32_t)k, lt = 0;
+  // this thread's candidates c = threadIdx.x + j * kSelThreads
+  uint32_t key[kSelRegs];
+#pragma unroll
+  for (int j = 0; j < kSelRegs; ++j) {
+    const int c = threadIdx.x + j * kSelThreads;
+    key[j] = c < n_cand ? desc_key(__ldcg(sc + c)) : 0xffffffffu;
+  }
+  const int n_reg = min(n_cand, kSelRegs * kSelThreads);
+
+  uint32_t prefix = 0, krem = (uint32_t)k;
   if (k > 0 && k < n_cand) {
-    // radix select of the k-th smallest desc_key, 8 bits at a time from the top
+    // radix select of the k-th smallest key, 8 bits at a time from the top;
+    // lanes with the same bucket add their count with one atomic
     for (int digit = 3; digit >= 0; --digit) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      if (threadIdx.x < 256) hist[threadIdx.x] = 0;
       __syncthreads();
       const int shift = digit * 8;
       const uint32_t hi_mask = digit == 3 ? 0u : (0xffffffffu << (shift + 8));
-      for (int c = threadIdx.x; c < n_cand; c += blockDim.x) {
-        uint32_t key = desc_key(__ldg(sc + c));
-        if ((key & hi_mask) == (prefix & hi_mask))
-          atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      auto count = [&](uint32_t kk, bool valid) {
+        const bool in = valid && (kk & hi_mask) == (prefix & hi_mask);
+        const uint32_t bucket = in ? (kk >> shift) & 255u : 256u;
+        const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], (uint32_t)__popc(peers));
+      };
+#pragma unroll
+      for (int j = 0; j < kSelRegs; ++j)
+        count(key[j], (int)threadIdx.x + j * kSelThreads < n_reg);
+      for (int c0 = n_reg; c0 < n_cand; c0 += kSelThreads) {
+        const int c = c0 + threadIdx.x;
+        count(c < n_cand ? desc_key(__ldcg(sc + c)) : 0u, c < n_cand);
       }
       __syncthreads();
       if (threadIdx.x < 32) {
-        // find bucket where the running count reaches krem (warp scan of 256)
-        const int lane = threadIdx.x;
+        // the bucket where the running count reaches krem (warp scan of 256)
         uint32_t cnt[8], loc = 0;
         for (int i = 0; i < 8; ++i) { cnt[i] = hist[lane * 8 + i]; loc += cnt[i]; }
         uint32_t incl = loc;
@@ -153,25 +179,33 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
         if (lane == 0) {
           s_prefix = prefix | ((uint32_t)fb << shift);
           s_krem = krem - bl;
-          s_lt = lt + bl;
         }
       }
       __syncthreads();
-      prefix = s_prefix; krem = s_krem; lt = s_lt;
+      prefix = s_prefix; krem = s_krem;
     }
   }
-  // write ascending ids of selected candidates
+  // ascending ids of the selected candidates: every key below the k-th, and
+  // the first krem (by index) of the keys equal to it
   int out_pos = 0, eq_seen = 0;
   for (int c0 = 0; c0 < n_cand; c0 += blockDim.x) {
     const int c = c0 + threadIdx.x;
+    const int jj = c0 / kSelThreads;
     int take = 0, eq = 0;
     if (c < n_cand) {
       if (k >= n_cand) {
         take = 1;
       } else if (k > 0) {
-        uint32_t key = desc_key(__ldg(sc + c));
-        if (key < prefix) take = 1;
-        else if (key == prefix) eq = 1;
+        uint32_t kk = 0;
+        if (jj < kSelRegs) {
+#pragma unroll
+          for (int j = 0; j < kSelRegs; ++j)
+            if (j == jj) kk = key[j];
+        } else {
+          kk = desc_key(__ldcg(sc + c));
+        }
+        if (kk < prefix) take = 1;
+        else if (kk == prefix) eq = 1;
       }
     }
     int eq_tot;
@@ -185,7 +219,6 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
   }
   for (int i = k + threadIdx.x; i < a.top_k; i += blockDim.x) ids[i] = -1;
   if (threadIdx.x == 0) a.out_len[b] = k * a.chunk_size + (L - ws);
-  (void)lt;
 }
 
 // Packed pairs of fp32 and their conversion to a bf16 pair.
@@ -330,24 +363,33 @@ DS_DEV void put_row(const GatherKArgs& a, const int b, const int i, const int pg
 template <int D>
 __global__ void __launch_bounds__(256) gather_rows(GatherKArgs a) {
   __shared__ __align__(16) float2 s_cs[8][D / 2];
+  grid_dep_launch_dependents();
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + warp;
-  if (i >= a.capacity) return;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= a.capacity) return;
   int L = __ldg(a.ctx_lens + b);
   if (L < 0 || (int64_t)L > (int64_t)a.max_pages * a.page_size ||
       (L + a.chunk_size - 1) / a.chunk_size > a.max_chunks)
     L = 0;
   const int ws = max(0, L - a.window);
-  const int n = __ldg(a.out_len + b);
+  // the sizes topk_select writes, formed here from the context length
+  const int k = min(a.top_k, ws / a.chunk_size);
+  const int sel_tokens = k * a.chunk_size;
+  const int n = sel_tokens + (L - ws);
+  // Rows are taken from the window region first (rows top_k * C .. of the
+  // full-size layout, then wrapping to 0), so the first CTAs copy the recent
+  // window, which does not depend on the selection, while topk_select still
+  // runs; rows of selected chunks wait for it.
+  const int i = (int)(((int64_t)r + (int64_t)a.top_k * a.chunk_size) % a.capacity);
   int32_t* posrow = a.out_positions + (int64_t)b * a.capacity;
   if (i >= n) {
     if (lane == 0) posrow[i] = -1;
     return;
   }
-  const int sel_tokens = n - (L - ws);
   int t;
   if (i < sel_tokens) {
+    grid_dep_wait();                // the selection comes from topk_select
     int c = __ldg(a.out_chunk_ids + (int64_t)b * a.top_k + i / a.chunk_size);
     t = c * a.chunk_size + i % a.chunk_size;
   } else {
@@ -387,15 +429,12 @@ cudaError_t launch_topk_gather(const ds_gather_args& g, cudaStream_t stream) {
   a.status = static_cast<uint32_t*>(g.workspace);
   a.rope_base = g.rope_base;
   set_rope_turns(a, g.rope_base, g.head_dim);
-  topk_select<<<g.batch, kSelThreads, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(topk_select, dim3(g.batch), dim3(kSelThreads), 0, stream, a);
   if (e != cudaSuccess) return e;
   dim3 grid((g.capacity + 7) / 8, g.batch);
   if (g.head_dim == 128)
-    gather_rows<128><<<grid, 256, 0, stream>>>(a);
-  else
-    gather_rows<64><<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+    return launch_dependent(gather_rows<128>, grid, dim3(256), 0, stream, a);
+  return launch_dependent(gather_rows<64>, grid, dim3(256), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------
