@@ -80,6 +80,90 @@ DS_DEV SeqPlan seq_sizes(const PlanArgs& a, int b, bool report) {
   return s;
 }
 
+// Plan at tiles-per-split t (all 32 lanes of one warp): the prefix of items
+// over the sequences, and the sequence asked for.
+static __device__ __noinline__ Plan plan_at(const PlanArgs& a, int b_sel, int item_sel, int t) {
+  const int lane = threadIdx.x & 31;
+  Plan p;
+  p.tps = t;
+  p.b = -1;
+  p.seq = SeqPlan{0, 0, 0, 0, 0, 0, 0, 0};
+  int32_t base = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    int b = b0 + lane;
+    SeqPlan s{0, 0, 0, 0, 0, 0, 0, 0};
+    int32_t items = 0;
+    if (b < a.batch) {
+      s = seq_sizes(a, b, false);
+      s.splits = (s.tiles + t - 1) / t;
+      items = a.num_kv_heads * s.rg * s.splits;
+    }
+    int32_t incl = items;
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    s.item_base = base + incl - items;
+    bool hit = (b < a.batch) &&
+               ((b_sel >= 0) ? (b == b_sel)
+                             : (item_sel >= s.item_base && item_sel < s.item_base + items));
+    unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      int src = __ffs(m) - 1;
+      p.b = __shfl_sync(0xffffffffu, b, src);
+      p.seq.L = __shfl_sync(0xffffffffu, s.L, src);
+      p.seq.T = __shfl_sync(0xffffffffu, s.T, src);
+      p.seq.node0 = __shfl_sync(0xffffffffu, s.node0, src);
+      p.seq.tiles = __shfl_sync(0xffffffffu, s.tiles, src);
+      p.seq.rows = __shfl_sync(0xffffffffu, s.rows, src);
+      p.seq.rg = __shfl_sync(0xffffffffu, s.rg, src);
+      p.seq.splits = __shfl_sync(0xffffffffu, s.splits, src);
+      p.seq.item_base = __shfl_sync(0xffffffffu, s.item_base, src);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  p.total_items = base;
+  return p;
+}
+
+// Splits round up per (sequence, kv head, row group), so ceil(total /
+// target) tiles per split can need more items than there are CTAs, and the
+// extra items would run as a second wave.  When the plan p does, this takes
+// instead the smallest tiles-per-split whose items fit (when any does).
+static __device__ __noinline__ Plan plan_refit(const PlanArgs& a, int b_sel, int item_sel,
+                                               Plan p) {
+  const int lane = threadIdx.x & 31;
+  auto items_for = [&](int32_t t, int32_t& max_tiles) {
+    int32_t it = 0;
+    max_tiles = 0;
+    for (int b0 = 0; b0 < a.batch; b0 += 32) {
+      const int b = b0 + lane;
+      int32_t v = 0, mt = 0;
+      if (b < a.batch) {
+        const SeqPlan s = seq_sizes(a, b, false);
+        v = a.num_kv_heads * s.rg * ((s.tiles + t - 1) / t);
+        mt = s.tiles;
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+        mt = max(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      }
+      it += v;
+      max_tiles = max(max_tiles, mt);
+    }
+    return it;
+  };
+  int32_t max_tiles, unused;
+  items_for(p.tps, max_tiles);
+  if (max_tiles <= p.tps || items_for(max_tiles, unused) > a.target_ctas) return p;
+  int32_t lo = p.tps, hi = max_tiles;   // items(lo) > target >= items(hi)
+  while (hi - lo > 1) {
+    const int32_t mid = lo + (hi - lo) / 2;
+    if (items_for(mid, unused) <= a.target_ctas) hi = mid; else lo = mid;
+  }
+  return plan_at(a, b_sel, item_sel, hi);
+}
+
 // Must be called by all 32 lanes of one warp.  Finds the sequence with index
 // b_sel (if b_sel >= 0) or the one owning work item item_sel.
 DS_DEV Plan plan_find(const PlanArgs& a, int b_sel, int item_sel) {
@@ -137,6 +221,7 @@ DS_DEV Plan plan_find(const PlanArgs& a, int b_sel, int item_sel) {
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
   p.total_items = base;
+  if (p.total_items > a.target_ctas) p = plan_refit(a, b_sel, item_sel, p);
   return p;
 }
 
