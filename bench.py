@@ -43,7 +43,7 @@ METRIC = ("µs/verify-step/layer and KV GB/s (% HBM peak) at 128K ctx, "
 UNIT = "us/verify-step/layer"
 DEFAULT_WORKLOAD = "llama8b-128k-32l"
 FALLBACK_HBM_GBS = 6800.0
-EV_EVERY = 4          # split-pass events bracket every 4th layer's launch
+EV_PER_STEP = 1       # split-pass launches bracketed by events per step
 CPU_BASELINE_LAYERS = 4   # whole layers the CPU baseline times
 
 
@@ -125,13 +125,14 @@ class ClockSampler:
         return parse_clock_samples(lines, t0, t1)
 
 
-def sampled_launches(steps: int, layers: int, every: int):
-    """(step, layer) pairs whose split pass is bracketed by events: layer l
-    of step s when l = s (mod every), so each layer is sampled in one step of
-    every `every` (all layers when there are fewer than `every`)."""
-    if layers <= every:
+def sampled_launches(steps: int, layers: int, per_step: int):
+    """(step, layer) pairs whose split pass is bracketed by events:
+    `per_step` consecutive layers per step, starting at layer s * per_step
+    (mod layers) in step s, so the sample rotates through every layer (all
+    layers of a step when it has no more than `per_step`)."""
+    if layers <= per_step:
         return [(s, l) for s in range(steps) for l in range(layers)]
-    return [(s, l) for s in range(steps) for l in range(layers) if l % every == s % every]
+    return [(s, (s * per_step + j) % layers) for s in range(steps) for j in range(per_step)]
 
 
 def parse_clock_samples(lines, t0=None, t1=None):
@@ -295,8 +296,8 @@ def _config(wl, st, kv_layout="NHD"):
             "chunk_size": wl.chunk_size, "top_k": wl.top_k,
             "window": wl.window, "vocab": wl.vocab, "accept": wl.accept,
             "rope_base": wl.rope_base, "kv_commit": True,
-            "split_events": f"every {EV_EVERY}th layer's split pass, "
-                            "rotating with the step",
+            "split_events": f"{EV_PER_STEP} split pass per step bracketed by events, "
+                            "the layer rotating with the step",
             "l2": "inputs larger than L2: every layer has its own "
                   f"{_kv_bytes(wl, st) / 1e6:.0f} MB K/V cache"}
 
@@ -490,10 +491,10 @@ def run_ours(args, wl, rank, world, local_rank):
                       kv_layout=args.kv_layout, with_commit=True,
                       rope_base=wl.rope_base)
     # events around a sample of the split-pass launches (each event pair
-    # sits between two kernels of the step and costs it a few
-    # microseconds): every EV_EVERY-th layer, rotating with the step so that
-    # every layer is sampled equally often
-    sampled = sampled_launches(args.steps, wl.layers, EV_EVERY)
+    # sits between two kernels of the step, breaks their dependent launch
+    # and costs the step a few microseconds): EV_PER_STEP launches per step,
+    # the layer rotating with the step so that the sample covers the layers
+    sampled = sampled_launches(args.steps, wl.layers, EV_PER_STEP)
     evs = [(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in sampled]
     for e_a, e_b in evs:      # torch creates the CUDA event on first record

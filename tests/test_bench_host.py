@@ -36,13 +36,15 @@ def test_garbage_lines_ignored():
     assert bench.parse_clock_samples(["", "bad line\n"], 0.0, 1.0) is None
 
 
-def test_sampled_launches_cover_every_layer_equally():
-    got = bench.sampled_launches(8, 32, 4)
-    assert len(got) == 8 * 8
+def test_sampled_launches_rotate_through_the_layers():
+    got = bench.sampled_launches(64, 32, 1)
+    assert len(got) == 64
+    assert [l for _, l in got] == [s % 32 for s in range(64)]
     per_layer = {}
-    for s, l in got:
-        assert l % 4 == s % 4
+    for _, l in got:
         per_layer[l] = per_layer.get(l, 0) + 1
     assert sorted(per_layer) == list(range(32)) and set(per_layer.values()) == {2}
-    assert bench.sampled_launches(3, 1, 4) == [(0, 0), (1, 0), (2, 0)]
+    two = bench.sampled_launches(3, 32, 2)
+    assert two == [(0, 0), (0, 1), (1, 2), (1, 3), (2, 4), (2, 5)]
+    assert bench.sampled_launches(3, 1, 1) == [(0, 0), (1, 0), (2, 0)]
     assert len(bench.sampled_launches(5, 3, 4)) == 15
