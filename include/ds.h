@@ -158,7 +158,13 @@ typedef struct ds_verify_args {
   int32_t out_dtype;            /* ds_out_dtype                                */
   float*  chunk_scores;         /* [batch, max_chunks] fp32                    */
   int32_t max_chunks;           /* row length of chunk_scores                  */
-  int32_t accumulate_scores;    /* 0: overwrite, 1: add (sum over layers)      */
+  int32_t accumulate_scores;    /* 0: overwrite, 1: add (sum over layers).
+                                   With 1 the call is a later layer of the
+                                   step that began with 0: ctx_lens and
+                                   tree_offsets must hold the same values and
+                                   must not be written by the kernel issued
+                                   right before this call on `stream` (they
+                                   are read while that kernel may still run) */
   int32_t num_sms;              /* CTAs to plan for; 0 = the device's SM count */
   void*   workspace;            /* scratch, >= ds_verify_attn_workspace_size   */
   size_t  workspace_bytes;

@@ -357,7 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- set-up
   // Barriers and tensor memory touch no global memory, so they are set up
   // before waiting for the preceding kernel of the stream; everything that
-  // reads the call's inputs comes after the wait.
+  // reads the call's inputs comes after the wait, except, for a call that
+  // accumulates scores (a later layer of the same step), the work plan: its
+  // inputs (lengths, tree offsets) are the step's, which the kernel right
+  // before such a call does not write, so the search overlaps its tail.
   if (warp == 1 && lane == 0) {
     mbar_init(bar(kQFull), 1);
     for (int s = 0; s < 6; ++s) {
@@ -381,9 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(&ctrl->tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  const bool early_plan = a.accumulate != 0;
+  if (early_plan && warp == 0) {
+    Plan p = plan_find(a.plan, -1, blockIdx.x);
+    if (lane == 0) ctrl->plan = p;
+  }
   grid_dep_wait();
   grid_dep_launch_dependents();
-  if (warp == 0) {
+  if (!early_plan && warp == 0) {
     Plan p = plan_find(a.plan, -1, blockIdx.x);
     if (lane == 0) ctrl->plan = p;
   }
