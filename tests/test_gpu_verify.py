@@ -103,6 +103,23 @@ def test_many_small_sms():
         H.assert_scores_close(step.scores, s, st, wl, f"sms={sms}")
 
 
+def test_plan_fitted_to_the_ctas():
+    """Per-sequence rounding of the split count overflows the CTAs here (14
+    items at 7 tiles per split for 12 CTAs), so the plan refits to 8 tiles
+    per split and 12 items; two layers, the second accumulating scores
+    (its plan is formed before the wait on the preceding kernel)."""
+    wl = synth.tiny_workload(batch=4, layers=2)
+    st, inp, mode = H.build_case(wl, layers=2, ctx_lens=(300, 2000, 700, 1500),
+                                 tree_sizes=(5, 9, 3, 7), seed=12)
+    step = _run_verify(wl, st, inp, mode, layers=2, num_sms=12)
+    total = 0
+    for l in range(2):
+        o, s, _ = H.oracle_layer(wl, st, inp, l, "NHD", step.max_chunks)
+        H.assert_attention_close(step.out[l], o, f"refit layer {l}")
+        total = total + s
+    H.assert_scores_close(step.scores, total, st, wl, "refit summed")
+
+
 @pytest.mark.parametrize("name", ["llama8b-32k", "llama8b-64k",
                                   "llama8b-128k-32l", "qwen3-8b-ragged-b8"])
 def test_full_size_one_layer(name):
