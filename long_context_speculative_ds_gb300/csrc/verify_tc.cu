@@ -885,9 +885,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (ctrl->last) {
-      // one row per thread; the splits' values sixteen loads at a time,
+      // one row per thread; the splits' values 32 loads at a time,
       // merged as a running (max, sum of 2^(x - max))
-      constexpr int kB = 16;
+      constexpr int kB = 32;
       for (int r = threadIdx.x; r < rows_here; r += kThreads) {
         const float* lp = a.lse_part + base * kRowsPerGroup + r;
         float mx = -CUDART_INF_F, sum = 0.f;
