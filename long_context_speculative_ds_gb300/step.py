@@ -181,16 +181,22 @@ class VerifyStep:
     def run_from_host(self, host: "StepInputs", host_out: dict):
         """One step end to end from pinned host inputs, with the copies on a
         side stream: the tree, then each layer's Q, then the logits, each
-        behind an event that only the kernels reading it wait on, so the
-        copies of later layers and of the logits overlap the verify of
+        group behind an event that only the kernels reading it wait on, so
+        the copies of later layers and of the logits overlap the verify of
         earlier layers.  The side stream first waits for the current stream
         (the previous step's kernels may still read these buffers).
+
+        A wait on an event between two kernels of the step breaks their
+        dependent launch, so there are few: layer 0 waits for the tree and
+        its Q, layer 1 for its Q, layer 2 for every remaining layer's Q (a
+        Q copy takes a few microseconds, a layer's verify over a hundred, so
+        they are done by then), and acceptance for the logits.
         Returns (host-to-device bytes, device-to-host bytes)."""
         comp = torch.cuda.current_stream()
         if getattr(self, "_copy_stream", None) is None:
             self._copy_stream = torch.cuda.Stream()
             self._ev_tree = torch.cuda.Event()
-            self._ev_q = [torch.cuda.Event() for _ in range(self.layers)]
+            self._ev_q = [torch.cuda.Event() for _ in range(3)]
             self._ev_acc = torch.cuda.Event()
         cp = self._copy_stream
         cp.wait_stream(comp)
@@ -209,7 +215,8 @@ class VerifyStep:
             self._ev_tree.record(cp)
             for l in range(self.layers):
                 put(d.q[l], host.q[l])
-                self._ev_q[l].record(cp)
+                if l < 2 or l == self.layers - 1:
+                    self._ev_q[min(l, 2)].record(cp)
             put(d.target_logits, host.target_logits)
             put(d.draft_tokens, host.draft_tokens)
             if d.draft_logits is not None:
@@ -219,7 +226,8 @@ class VerifyStep:
             self._ev_acc.record(cp)
         comp.wait_event(self._ev_tree)
         for l in range(self.layers):
-            comp.wait_event(self._ev_q[l])
+            if l <= 2:
+                comp.wait_event(self._ev_q[l])
             self.verify_layer(l)
         self.gather()
         comp.wait_event(self._ev_acc)
@@ -227,6 +235,26 @@ class VerifyStep:
         if self.with_commit:
             self.commit()
         return n, self.download(host_out)
+
+    def capture_from_host(self, host: "StepInputs", host_out: dict):
+        """Capture one end-to-end step (`run_from_host`: the copies in, every
+        kernel, the copies out) as a CUDA graph; `replay` then runs the whole
+        step again with one launch, from whatever the pinned host buffers
+        hold at that time.  Buffers, sizes and the library's arguments are
+        those of the capture.  Call it after one eager `run_from_host`: the
+        library sets function attributes on first use, which a stream
+        capture does not allow.  Returns what `run_from_host` returns."""
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            self._graph_bytes = self.run_from_host(host, host_out)
+        self._graph = graph
+        return self._graph_bytes
+
+    def replay(self):
+        """One end-to-end step through the captured graph (asynchronous on
+        the current stream).  Returns (host-to-device, device-to-host) bytes."""
+        self._graph.replay()
+        return self._graph_bytes
 
     def download(self, host_out: dict):
         """Copy the step's small results (accepted path, count, bonus, chosen
