@@ -77,6 +77,18 @@ def test_many_random_trees(mode, vocab):
     assert exempt <= 1
 
 
+@pytest.mark.parametrize("mode", ["greedy", "reject"])
+def test_vocabulary_beyond_the_register_slices(mode):
+    """A vocabulary whose per-CTA slice exceeds what the rejection node pass
+    holds in registers and shared memory (here 200,000 > 163,840 tokens) takes
+    the streaming node pass; greedy runs its usual argmax pass."""
+    wl = synth.tiny_workload(batch=3, vocab=200000, max_depth=6, max_branch=3)
+    st, inp, _ = H.build_case(wl, mode=mode, seed=7, ctx_lens=[32] * 3,
+                              tree_sizes=[9, 1, 14], draft="noisy")
+    step = H.make_step(wl, inp, mode)
+    assert _check(st, inp, step, mode)[1] <= 1
+
+
 def test_one_hot_target_rejection_equals_greedy():
     wl = synth.tiny_workload(batch=6, vocab=300, max_depth=6, max_branch=3)
     st, inp, _ = H.build_case(wl, mode="reject", seed=21,
