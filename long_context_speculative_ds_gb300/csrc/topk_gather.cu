@@ -121,19 +121,19 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
   const float* sc = a.scores + (int64_t)b * a.max_chunks;
   int32_t* ids = a.out_chunk_ids + (int64_t)b * a.top_k;
 
-  // this thread's candidates c = threadIdx.x + j * kSelThreads
+  // this thread's candidates c = kSelRegs * threadIdx.x + j (consecutive,
+  // so that the selected ids leave in order with one scan per pass)
   uint32_t key[kSelRegs];
 #pragma unroll
   for (int j = 0; j < kSelRegs; ++j) {
-    const int c = threadIdx.x + j * kSelThreads;
+    const int c = kSelRegs * (int)threadIdx.x + j;
     key[j] = c < n_cand ? desc_key(__ldcg(sc + c)) : 0xffffffffu;
   }
   const int n_reg = min(n_cand, kSelRegs * kSelThreads);
 
   uint32_t prefix = 0, krem = (uint32_t)k;
   if (k > 0 && k < n_cand) {
-    // radix select of the k-th smallest key, 8 bits at a time from the top;
-    // lanes with the same bucket add their count with one atomic
+    // radix select of the k-th smallest key, 8 bits at a time from the top
     for (int digit = 3; digit >= 0; --digit) {
       if (threadIdx.x < 256) hist[threadIdx.x] = 0;
       __syncthreads();
@@ -142,12 +142,11 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
       auto count = [&](uint32_t kk, bool valid) {
         const bool in = valid && (kk & hi_mask) == (prefix & hi_mask);
         const uint32_t bucket = in ? (kk >> shift) & 255u : 256u;
-        const unsigned peers = __match_any_sync(0xffffffffu, bucket);
-        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], (uint32_t)__popc(peers));
+        if (in) atomicAdd(&hist[bucket], 1u);
       };
 #pragma unroll
       for (int j = 0; j < kSelRegs; ++j)
-        count(key[j], (int)threadIdx.x + j * kSelThreads < n_reg);
+        count(key[j], kSelRegs * (int)threadIdx.x + j < n_reg);
       for (int c0 = n_reg; c0 < n_cand; c0 += kSelThreads) {
         const int c = c0 + threadIdx.x;
         count(c < n_cand ? desc_key(__ldcg(sc + c)) : 0u, c < n_cand);
@@ -186,28 +185,49 @@ __global__ void __launch_bounds__(kSelThreads) topk_select(GatherKArgs a) {
     }
   }
   // ascending ids of the selected candidates: every key below the k-th, and
-  // the first krem (by index) of the keys equal to it
-  int out_pos = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < n_cand; c0 += blockDim.x) {
-    const int c = c0 + threadIdx.x;
-    const int jj = c0 / kSelThreads;
-    int take = 0, eq = 0;
-    if (c < n_cand) {
-      if (k >= n_cand) {
-        take = 1;
-      } else if (k > 0) {
-        uint32_t kk = 0;
-        if (jj < kSelRegs) {
-#pragma unroll
-          for (int j = 0; j < kSelRegs; ++j)
-            if (j == jj) kk = key[j];
-        } else {
-          kk = desc_key(__ldcg(sc + c));
-        }
-        if (kk < prefix) take = 1;
-        else if (kk == prefix) eq = 1;
-      }
+  // the first krem (by index) of the keys equal to it.  The register-held
+  // candidates first (each thread's are consecutive: one scan of the ties,
+  // one of the positions), then any beyond them, kSelThreads at a time.
+  auto classify = [&](uint32_t kk, int& take, int& eq) {
+    take = eq = 0;
+    if (k >= n_cand) take = 1;
+    else if (k > 0) {
+      if (kk < prefix) take = 1;
+      else if (kk == prefix) eq = 1;
     }
+  };
+  int out_pos = 0, eq_seen = 0;
+  {
+    int take[kSelRegs], eq[kSelRegs], n_eq = 0;
+#pragma unroll
+    for (int j = 0; j < kSelRegs; ++j) {
+      take[j] = eq[j] = 0;
+      if (kSelRegs * (int)threadIdx.x + j < n_reg) classify(key[j], take[j], eq[j]);
+      n_eq += eq[j];
+    }
+    int eq_tot;
+    int eq_rank = block_excl_scan(n_eq, s_warp, &eq_tot);
+    int n_take = 0;
+#pragma unroll
+    for (int j = 0; j < kSelRegs; ++j) {
+      if (eq[j]) {
+        if ((uint32_t)eq_rank < krem) take[j] = 1;
+        ++eq_rank;
+      }
+      n_take += take[j];
+    }
+    eq_seen = eq_tot;
+    int take_tot;
+    int pos = block_excl_scan(n_take, s_warp, &take_tot);
+#pragma unroll
+    for (int j = 0; j < kSelRegs; ++j)
+      if (take[j]) ids[pos++] = kSelRegs * (int)threadIdx.x + j;
+    out_pos = take_tot;
+  }
+  for (int c0 = n_reg; c0 < n_cand; c0 += kSelThreads) {
+    const int c = c0 + threadIdx.x;
+    int take = 0, eq = 0;
+    if (c < n_cand) classify(desc_key(__ldcg(sc + c)), take, eq);
     int eq_tot;
     int eq_rank = block_excl_scan(eq, s_warp, &eq_tot) + eq_seen;
     if (eq && (uint32_t)eq_rank < krem) take = 1;
