@@ -29,7 +29,8 @@ struct VerifyLayout {
   size_t counters;      // [batch][kv][rg_max] u32           splits finished (0 between calls)
   size_t gdesc;         // [batch][kv][rg_max] int4          first item and splits of the
                         //                                   row group (by its last split)
-  size_t o_part;        // [max_items][256][head_dim] f32   split outputs (normalised)
+  size_t o_part;        // [max_items][256][head_dim] split outputs (normalised), bf16
+                        // when the output is bf16, else f32 (sized for f32)
   size_t lse_part;      // [max_items][256] f32              split log2-sum-exp
   size_t clse;          // [batch][kv][rg_max][max_chunks][256] f32 chunk log2 mass
   size_t row_lse;       // [batch][kv][rg_max][256] f32      final row log2-sum-exp

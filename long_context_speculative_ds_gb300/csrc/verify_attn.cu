@@ -38,22 +38,26 @@ namespace ds {
 // combine (the first n_comb CTAs): one warp per (sequence, kv head, row
 //   group, row).  The sequence's sizes and the row group's descriptor (its
 //   first split item and split count, written by its last split) come in one
-//   round trip; then the outputs of kCombBatch splits at a time (lane-
-//   parallel over columns) together with their log2-sum-exps (lane-parallel
-//   over splits) and the row's final log2-sum-exp; the weights 2^{lse_s -
-//   lse} are broadcast from the lane that holds split s.  The batch keeps the
-//   kernel within 64 registers, so that every CTA of the launch is resident
-//   at once.
+//   round trip; then the outputs of a batch of splits (lane-parallel over
+//   columns) together with their log2-sum-exps (lane-parallel over splits)
+//   and the row's final log2-sum-exp; the weights 2^{lse_s - lse} are
+//   broadcast from the lane that holds split s.  The split outputs are bf16
+//   when the final output is (f32 otherwise), and a batch is 20 bf16 splits
+//   (head_dim 128) or kCombBatch f32 splits: within 64 registers, so that
+//   every CTA of the launch is resident at once, and at 128K context (19
+//   splits per row group) the bf16 batch is a single round trip.
 // finalize (the rest): one warp per (chunk, sequence).  Lane i covers rows
 //   4i .. 4i + 3 and 128 + 4i .. 128 + 4i + 3 of every (kv head, row group)
-//   with 16-byte loads; kFinCombos (kv head, row group) combinations per
-//   round.
+//   with 16-byte loads of the chunk masses, kFinCombos (kv head, row group)
+//   combinations per round; the rows' final log2-sum-exps, the same for
+//   every chunk of the sequence, are read through L1 as each round is
+//   summed.
 constexpr int kCombBatch = 8;
-constexpr int kFinCombos = 3;   // (kv head, row group) combinations per finalize round
+constexpr int kFinCombos = 4;   // (kv head, row group) combinations per finalize round
 constexpr int kFinishThreads = 256;
 constexpr int kFinishWarps = kFinishThreads / 32;
 
-template <int D>
+template <int D, bool HALF>
 DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   const int row_blocks = kRowsPerGroup / kFinishWarps;
   const int grp = blk / row_blocks, rblk = blk % row_blocks;
@@ -61,7 +65,7 @@ DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   const int b = grp / per_b;
   const int h = (grp / a.plan.rg_max) % a.plan.num_kv_heads;
   const int rgi = grp % a.plan.rg_max;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int r = rblk * kFinishWarps + warp;
   // sizes, descriptor and the row's final log2-sum-exp in one round trip
   const SeqPlan sq = seq_sizes(a.plan, b, false);
@@ -74,55 +78,10 @@ DS_DEV void combine_row(const VerifyKArgs& a, int blk) {
   const int grow = rgi * kRowsPerGroup + r;
   const int node = sq.node0 + grow / G;
   const int qh = h * G + grow % G;
-  const int base = gd.x;
-  const int ns = gd.y;
-  const float* lp = a.lse_part + (int64_t)base * kRowsPerGroup + r;
-  constexpr int E = D / 32;   // floats per lane (4 or 2)
-  const float* op0 = a.o_part + ((int64_t)base * kRowsPerGroup + r) * D + lane * E;
-  const int64_t sstride = (int64_t)kRowsPerGroup * D;
-
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += kCombBatch) {
-    float x[kCombBatch][E];
-#pragma unroll
-    for (int k = 0; k < kCombBatch; ++k) {
-      if (s0 + k < ns) {
-        const float* op = op0 + (int64_t)(s0 + k) * sstride;
-        if constexpr (E == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(op));
-          x[k][0] = v.x; x[k][1] = v.y; x[k][2] = v.z; x[k][3] = v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(op));
-          x[k][0] = v.x; x[k][1] = v.y;
-        }
-      }
-    }
-    // weight of split s0 + lane (lanes below kCombBatch), broadcast below
-    const float wl = (lane < kCombBatch && s0 + lane < ns)
-                         ? exp2f(__ldcg(lp + (int64_t)(s0 + lane) * kRowsPerGroup) - lse)
-                         : 0.f;
-#pragma unroll
-    for (int k = 0; k < kCombBatch; ++k) {
-      const float w = __shfl_sync(0xffffffffu, wl, k);
-      if (s0 + k < ns && w != 0.f) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
-      }
-    }
-  }
-  const int64_t obase = ((int64_t)node * a.num_q_heads + qh) * D + lane * E;
-  if (a.out_f32) {
-    float* out = reinterpret_cast<float*>(a.out) + obase;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = acc[e];
-  } else {
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + obase;
-#pragma unroll
-    for (int e = 0; e < E; e += 2)
-      *reinterpret_cast<__nv_bfloat162*>(out + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
-  }
+  // bf16 rows are half the registers, so with head_dim 128 twenty splits
+  // (and at 64, thirty-two) arrive in one round trip
+  constexpr int NB = HALF ? (D == 128 ? 20 : 32) : kCombBatch;
+  combine_row_splits<D, HALF, NB>(a, gd.x, gd.y, r, lse, (int64_t)node * a.num_q_heads + qh);
 }
 
 DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
@@ -138,7 +97,9 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
   // masked once the sizes are known.
   const int rg_max = a.plan.rg_max;
   const int combos = a.plan.num_kv_heads * rg_max;
-  float4 v[kFinCombos][2], w[kFinCombos][2];
+  const float4* rl_b =
+      reinterpret_cast<const float4*>(a.row_lse + (int64_t)b * combos * kRowsPerGroup);
+  float4 v[kFinCombos][2];
   auto load = [&](int cb0) {
 #pragma unroll
     for (int k = 0; k < kFinCombos; ++k) {
@@ -146,35 +107,39 @@ DS_DEV void finalize_chunk(const VerifyKArgs& a, int blk) {
         const int64_t hb = (int64_t)b * combos + cb0 + k;
         const float4* cl = reinterpret_cast<const float4*>(
             a.clse + (hb * a.plan.max_chunks + c) * kRowsPerGroup);
-        const float4* rl = reinterpret_cast<const float4*>(a.row_lse + hb * kRowsPerGroup);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          v[k][q] = __ldcg(cl + lane + 32 * q);
-          w[k][q] = __ldg(rl + lane + 32 * q);
-        }
+        for (int q = 0; q < 2; ++q) v[k][q] = __ldcg(cl + lane + 32 * q);
       }
     }
   };
   load(0);
-  const SeqPlan sq = seq_sizes(a.plan, b, false);
-  const int n_ch = (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size;
-  if (c >= n_ch) return;
+  int rows, rg;
+  {
+    const SeqPlan sq = seq_sizes(a.plan, b, false);
+    if (c >= (sq.L + a.plan.chunk_size - 1) / a.plan.chunk_size) return;
+    rows = sq.rows;
+    rg = sq.rg;
+  }
   float sum = 0.f;
   for (int cb0 = 0; cb0 < combos; cb0 += kFinCombos) {
     if (cb0 > 0) load(cb0);
 #pragma unroll
     for (int k = 0; k < kFinCombos; ++k) {
-      const int rgi = (cb0 + k) % rg_max;
-      if (cb0 + k < combos && rgi < sq.rg) {
-        const int rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
+      const int cb = cb0 + k;
+      const int rgi = cb % rg_max;
+      if (cb < combos && rgi < rg) {
+        // rows of this lane below the row group's end
+        const int left = rows - rgi * kRowsPerGroup - 4 * lane;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int r0 = 4 * lane + 128 * q;
-          const float vv[4] = {v[k][q].x, v[k][q].y, v[k][q].z, v[k][q].w};
-          const float ww[4] = {w[k][q].x, w[k][q].y, w[k][q].z, w[k][q].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (r0 + e < rows_here) sum += exp2f(vv[e] - ww[e]);
+          // the sequence's row log2-sum-exps are the same 8 KB for every
+          // warp of the sequence: read through L1 when the masses are in
+          const float4 w = __ldg(rl_b + cb * (kRowsPerGroup / 4) + lane + 32 * q);
+          const int n = left - 128 * q;
+          if (n > 0) sum += exp2f(v[k][q].x - w.x);
+          if (n > 1) sum += exp2f(v[k][q].y - w.y);
+          if (n > 2) sum += exp2f(v[k][q].z - w.z);
+          if (n > 3) sum += exp2f(v[k][q].w - w.w);
         }
       }
     }
@@ -190,8 +155,13 @@ template <int D>
 __global__ void __launch_bounds__(kFinishThreads, 4) verify_finish(VerifyKArgs a, int n_comb) {
   grid_dep_wait();
   grid_dep_launch_dependents();
-  if ((int)blockIdx.x < n_comb) combine_row<D>(a, blockIdx.x);
-  else finalize_chunk(a, blockIdx.x - n_comb);
+  if ((int)blockIdx.x < n_comb) {
+    // split outputs are bf16 when the final output is
+    if (a.out_f32) combine_row<D, false>(a, blockIdx.x);
+    else combine_row<D, true>(a, blockIdx.x);
+  } else {
+    finalize_chunk(a, blockIdx.x - n_comb);
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -77,7 +77,8 @@ enum Bar {
                    // seen the first
   kORdy = 27,      // [group]: one completion per issued P V
   kOFinal = 29,    // [group]: all of the group's MMAs have completed
-  kNumBars = 31
+  kAnc = 31,       // the tree's ancestor masks are in ctrl->anc (warp 1)
+  kNumBars = 32
 };
 
 struct Ctrl {
@@ -252,7 +253,8 @@ __device__ __noinline__ void write_row_output(const bool row_mode, const int g, 
                                               const float l, float* __restrict__ merge_buf,
                                               float* m1buf, float* l1buf,
                                               float* __restrict__ stage,
-                                              float* __restrict__ op_warp,
+                                              const bool part_bf16,
+                                              void* __restrict__ op_warp,
                                               float* __restrict__ lse_out) {
   using namespace ptx;
   const int lane = threadIdx.x & 31;
@@ -296,33 +298,88 @@ __device__ __noinline__ void write_row_output(const bool row_mode, const int g, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) r[i] = 0u;
     }
-    // this thread's row: 32 columns into the staging tile
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float o = __uint_as_float(r[i + e]) * sc0;
-        if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i + e) * 128 + lrow] * sc1;
-        v[e] = o * inv;
-      }
-      *reinterpret_cast<float4*>(stage + lane * kStageStride + 4 * ((i >> 2) ^ (lane & 7))) =
-          make_float4(v[0], v[1], v[2], v[3]);
+    for (int i = 0; i < 32; ++i) {
+      float o = __uint_as_float(r[i]) * sc0;
+      if (sc1 != 0.f) o += merge_buf[(c4 * 32 + i) * 128 + lrow] * sc1;
+      r[i] = __float_as_uint(o * inv);
     }
+    if (part_bf16) {
+      // bf16 pairs: a row's 32 columns are 64 bytes, four 16-byte chunks;
+      // chunk c of row q sits in the row's slot c ^ ((q / 2) % 4), so that
+      // eight lanes of one access (eight rows, or two rows' four chunks)
+      // touch distinct 16-byte bank groups
+      uint32_t* st = reinterpret_cast<uint32_t*>(stage) + lane * 16;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]),
+                             __uint_as_float(r[8 * c + 2 * e + 1]));
+        *reinterpret_cast<uint4*>(st + 4 * (c ^ ((lane >> 1) & 3))) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      __syncwarp();
+      // rows 8k + lane / 4, 16-byte chunk lane % 4 of the slice
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(op_warp);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = 8 * k + (lane >> 2), cc = lane & 3;
+        if (rr < rows_left) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              reinterpret_cast<const uint32_t*>(stage) + rr * 16 + 4 * (cc ^ ((rr >> 1) & 3)));
+          *reinterpret_cast<uint4*>(ob + (int64_t)rr * D + c4 * 32 + cc * 8) = v;
+        }
+      }
+      __syncwarp();
+      continue;
+    }
+    // f32: this thread's row, 32 columns, into the staging tile
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(stage + lane * kStageStride + 4 * ((i >> 2) ^ (lane & 7))) =
+          make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                      __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
     __syncwarp();
     // rows 4k + lane / 8, columns 4 (lane % 8) .. + 3 of the slice
+    float* of = reinterpret_cast<float*>(op_warp);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int rr = 4 * k + (lane >> 3), cc = 4 * (lane & 7);
       if (rr < rows_left) {
         const float4 v = *reinterpret_cast<const float4*>(
             stage + rr * kStageStride + 4 * ((lane & 7) ^ (rr & 7)));
-        *reinterpret_cast<float4*>(op_warp + (int64_t)rr * D + c4 * 32 + cc) = v;
+        *reinterpret_cast<float4*>(of + (int64_t)rr * D + c4 * 32 + cc) = v;
       }
     }
     __syncwarp();
   }
   if (row_ok) *lse_out = lt > 0.f ? mt + __log2f(lt) : -CUDART_INF_F;
+}
+
+// Final log2-sum-exp of one row from its ns splits' (lp[s * 256]): 32 loads
+// at a time, merged as a running (max, sum of 2^(x - max)).
+DS_DEV float row_lse_from_splits(const float* lp, int ns) {
+  constexpr int kB = 32;
+  float mx = -CUDART_INF_F, sum = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += kB) {
+    float v[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k)
+      v[k] = s0 + k < ns ? __ldcg(lp + (int64_t)(s0 + k) * kRowsPerGroup) : -CUDART_INF_F;
+    float bm = v[0];
+#pragma unroll
+    for (int k = 1; k < kB; ++k) bm = fmaxf(bm, v[k]);
+    const float nm = fmaxf(mx, bm);
+    if (nm == -CUDART_INF_F) continue;
+    float add = 0.f;
+#pragma unroll
+    for (int k = 0; k < kB; ++k) add += exp2f(v[k] - nm);
+    sum = (mx == -CUDART_INF_F ? 0.f : sum * exp2f(mx - nm)) + add;
+    mx = nm;
+  }
+  return sum > 0.f ? mx + log2f(sum) : -CUDART_INF_F;
 }
 
 template <int D>
@@ -375,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 4; ++s) mbar_init(bar(kSFull + s), 1);
     for (int s = 0; s < 4; ++s) mbar_init(bar(kPFull + s), 128);
     for (int s = 0; s < 2; ++s) mbar_init(bar(kOFinal + s), 1);
+    mbar_init(bar(kAnc), 32);
     ctrl->abort = 0;
     for (int i = 0; i < 5; ++i) ctrl->where[i] = 0;
     fence_mbar_init();
@@ -421,52 +479,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = sq.L, T = sq.T;
   const bool need_anc = active && t1 * kTileKeys > L;
 
-  if (need_anc && warp == 0) {
-    // ancestor masks of all nodes of this tree, by pointer doubling
-    for (int j = lane; j < T; j += 32) ctrl->parents[j] = __ldg(a.parents + sq.node0 + j);
-    __syncwarp();
-    uint64_t m[2] = {0, 0};
-    int up[2] = {-1, -1};
-    for (int k = 0; k < 2; ++k) {
-      const int j = lane + 32 * k;
-      if (j < T) {
-        int pj = ctrl->parents[j];
-        bool ok = (j == 0) ? (pj == -1) : (pj >= 0 && pj < j);
-        if (!ok) {
-          flag(a.plan.status, DS_DEV_BAD_TREE);
-          pj = -1;
-        }
-        m[k] = (1ull << j) | (pj >= 0 ? (1ull << pj) : 0ull);
-        up[k] = pj;
-        ctrl->anc[j] = m[k];
-        ctrl->parents[j] = pj;   // sanitised jump pointer
-      }
-    }
-    __syncwarp();
-    for (int round = 0; round < 6; ++round) {
-      uint64_t add[2] = {0, 0};
-      int nup[2] = {-1, -1};
-      for (int k = 0; k < 2; ++k) {
-        const int j = lane + 32 * k;
-        if (j < T && up[k] >= 0) {
-          add[k] = ctrl->anc[up[k]];
-          nup[k] = ctrl->parents[up[k]];
-        }
-      }
-      __syncwarp();
-      for (int k = 0; k < 2; ++k) {
-        const int j = lane + 32 * k;
-        if (j < T) {
-          m[k] |= add[k];
-          up[k] = nup[k];
-          ctrl->anc[j] = m[k];
-          ctrl->parents[j] = nup[k];
-        }
-      }
-      __syncwarp();
-    }
-  }
-  __syncthreads();
 
   const int kslots = row_mode ? 2 : 3;
   const int klead = row_mode ? 1 : 2;
@@ -633,6 +645,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = max(0, nv - 3); n < nv; ++n)
           drain_wait(bar(full_bar(1, n)), full_par(1, n));
       }
+    } else if (warp == 1) {
+      // ---------------------------------------------------- ancestor masks
+      // Only the split that holds the tree's keys needs them, and only for
+      // its last tile(s): they are formed here, beside the loader, and the
+      // softmax warps wait for them (kAnc) just before the first unit that
+      // holds tree keys.
+      if (need_anc) {
+        // ancestor masks of all nodes of this tree, by pointer doubling
+        for (int j = lane; j < T; j += 32) ctrl->parents[j] = __ldg(a.parents + sq.node0 + j);
+        __syncwarp();
+        uint64_t m[2] = {0, 0};
+        int up[2] = {-1, -1};
+        for (int k = 0; k < 2; ++k) {
+          const int j = lane + 32 * k;
+          if (j < T) {
+            int pj = ctrl->parents[j];
+            bool ok = (j == 0) ? (pj == -1) : (pj >= 0 && pj < j);
+            if (!ok) {
+              flag(a.plan.status, DS_DEV_BAD_TREE);
+              pj = -1;
+            }
+            m[k] = (1ull << j) | (pj >= 0 ? (1ull << pj) : 0ull);
+            up[k] = pj;
+            ctrl->anc[j] = m[k];
+            ctrl->parents[j] = pj;   // sanitised jump pointer
+          }
+        }
+        __syncwarp();
+        for (int round = 0; round < 6; ++round) {
+          uint64_t add[2] = {0, 0};
+          int nup[2] = {-1, -1};
+          for (int k = 0; k < 2; ++k) {
+            const int j = lane + 32 * k;
+            if (j < T && up[k] >= 0) {
+              add[k] = ctrl->anc[up[k]];
+              nup[k] = ctrl->parents[up[k]];
+            }
+          }
+          __syncwarp();
+          for (int k = 0; k < 2; ++k) {
+            const int j = lane + 32 * k;
+            if (j < T) {
+              m[k] |= add[k];
+              up[k] = nup[k];
+              ctrl->anc[j] = m[k];
+              ctrl->parents[j] = nup[k];
+            }
+          }
+          __syncwarp();
+        }
+        mbar_arrive(bar(kAnc));
+      }
     } else if (warp == 2 || warp == 3) {
       // ------------------------------------------------------ MMA issuers
       // One issuing thread per softmax group (warp 2: group 0, warp 3:
@@ -756,7 +820,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = grow_local < rows_here;
       const int grow = rgi * kRowsPerGroup + grow_local;
       const int jn = grow / G;
-      const uint64_t anc = (need_anc && row_ok && jn < T) ? ctrl->anc[jn] : 0ull;
+      uint64_t anc = 0ull;          // read at the first unit with tree keys
+      bool anc_ready = !need_anc;
       const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
       const uint32_t tG = tmem + lane_addr + 256 * g;
       const uint32_t tO = tG + 128;
@@ -790,6 +855,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             softmax_unit<false>(tS, tP, ~0u, ~0u, ~0u, ~0u, c2, u == 0, m2, l, cs, alpha,
                                 rescale, tile_slot0, 4 * hb, cshift, n_ch, row_ok, clse_row);
           } else {
+            if (!anc_ready) {
+              if (lrow == 0) ctrl->where[2 + g] = 30000 + kAnc * 100;
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(kAnc), 0, abort_flag, diag,
+                                                     30000 + kAnc * 100));
+              if (!ok) break;
+              anc = (row_ok && jn < T) ? ctrl->anc[jn] : 0ull;
+              anc_ready = true;
+            }
             // column c is visible iff c < L - unit_slot0 (context) or it is
             // tree slot i = c - (L - unit_slot0) with bit i of the row's
             // ancestor mask set
@@ -849,9 +922,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* stage = reinterpret_cast<float*>(smem + (row_mode ? g * TB : 0)) +
                      q4 * 32 * kStageStride;
       const int warp_row0 = grow_local - lane;       // first row of this warp
+      // the split outputs are kept at the precision of the final output
+      const int64_t orow = ((int64_t)blockIdx.x * kRowsPerGroup + warp_row0) * D;
+      void* op_warp = a.out_f32 ? static_cast<void*>(a.o_part + orow)
+                                : static_cast<void*>(
+                                      reinterpret_cast<__nv_bfloat16*>(a.o_part) + orow);
       write_row_output<D>(row_mode, g, ok, nt1, tO, lrow, rows_here - warp_row0, m2, l,
-                          merge_buf, m1buf, l1buf, stage,
-                          a.o_part + ((int64_t)blockIdx.x * kRowsPerGroup + warp_row0) * D,
+                          merge_buf, m1buf, l1buf, stage, !a.out_f32, op_warp,
                           a.lse_part + (int64_t)blockIdx.x * kRowsPerGroup + grow_local);
     }
   }
@@ -864,12 +941,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (diag[1] == blockIdx.x)
       for (int i = 0; i < 5; ++i) diag[2 + i] = ctrl->where[i];
   }
-  // The last split of a (sequence, kv head, row group) to finish forms the
-  // rows' final log2-sum-exp from every split's, and records where the row
-  // group's splits are, so that the finish kernel can merge outputs and
-  // normalise chunk masses independently.  Every split counts (a timed-out
-  // one too), and the last resets the counter to zero for the next call.
   if (active && nt > 0) {
+    // The last split of a (sequence, kv head, row group) to finish forms
+    // the rows' final log2-sum-exp from every split's, and records where
+    // the row group's splits are, so that the finish kernel can merge
+    // outputs and normalise chunk masses independently.  Every split counts
+    // (a timed-out one too), and the last resets the counter to zero for
+    // the next call.
     const int64_t cidx = ((int64_t)p.b * a.plan.num_kv_heads + kvh) * a.plan.rg_max + rgi;
     const int64_t base = (int64_t)sq.item_base + (kvh * sq.rg + rgi) * sq.splits;
     if (threadIdx.x == 0) {
@@ -884,33 +962,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctrl->last = last;
     }
     __syncthreads();
-    if (ctrl->last) {
-      // one row per thread; the splits' values 32 loads at a time,
-      // merged as a running (max, sum of 2^(x - max))
-      constexpr int kB = 32;
-      for (int r = threadIdx.x; r < rows_here; r += kThreads) {
-        const float* lp = a.lse_part + base * kRowsPerGroup + r;
-        float mx = -CUDART_INF_F, sum = 0.f;
-        for (int s0 = 0; s0 < sq.splits; s0 += kB) {
-          float v[kB];
-#pragma unroll
-          for (int k = 0; k < kB; ++k)
-            v[k] = s0 + k < sq.splits ? __ldcg(lp + (int64_t)(s0 + k) * kRowsPerGroup)
-                                      : -CUDART_INF_F;
-          float bm = v[0];
-#pragma unroll
-          for (int k = 1; k < kB; ++k) bm = fmaxf(bm, v[k]);
-          const float nm = fmaxf(mx, bm);
-          if (nm == -CUDART_INF_F) continue;
-          float add = 0.f;
-#pragma unroll
-          for (int k = 0; k < kB; ++k) add += exp2f(v[k] - nm);
-          sum = (mx == -CUDART_INF_F ? 0.f : sum * exp2f(mx - nm)) + add;
-          mx = nm;
-        }
-        a.row_lse[cidx * kRowsPerGroup + r] = sum > 0.f ? mx + log2f(sum) : -CUDART_INF_F;
-      }
-    }
+    if (ctrl->last)
+      for (int r = threadIdx.x; r < rows_here; r += kThreads)
+        a.row_lse[cidx * kRowsPerGroup + r] =
+            row_lse_from_splits(a.lse_part + base * kRowsPerGroup + r, sq.splits);
   }
   if (warp == 1) {
     if (active && nt > 0 && lane == 0) {

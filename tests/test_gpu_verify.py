@@ -120,6 +120,29 @@ def test_plan_fitted_to_the_ctas():
     H.assert_scores_close(step.scores, total, st, wl, "refit summed")
 
 
+@pytest.mark.parametrize("sms", [0, 1000])
+def test_sequence_without_tree_nodes(sms):
+    """A sequence with no tree nodes has no work item: its chunks get zero
+    scores (entries past a sequence's chunks keep their old value), next to
+    sequences that do have trees, with the device's CTAs and with 1000
+    planned CTAs (one tile per item)."""
+    wl = synth.tiny_workload(batch=3)
+    st, inp, mode = H.build_case(wl, ctx_lens=(600, 300, 200), tree_sizes=(5, 0, 7),
+                                 seed=31)
+    step = H.make_step(wl, inp, mode, num_sms=sms)
+    step.scores.fill_(7.0)
+    step.verify_layer(0)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    o, s, _ = H.oracle_layer(wl, st, inp, 0, "NHD", step.max_chunks)
+    H.assert_attention_close(step.out[0], o, f"sms={sms}")
+    H.assert_scores_close(step.scores, s, st, wl, f"sms={sms}")
+    g = step.scores.cpu().numpy()
+    n1 = -(-300 // wl.chunk_size)
+    assert (g[1, :n1] == 0.0).all()
+    assert (g[1, n1:] == 7.0).all() and (g[2, -(-200 // wl.chunk_size):] == 7.0).all()
+
+
 @pytest.mark.parametrize("name", ["llama8b-32k", "llama8b-64k",
                                   "llama8b-128k-32l", "qwen3-8b-ragged-b8"])
 def test_full_size_one_layer(name):
