@@ -72,17 +72,20 @@ def test_edge_cases(name, over, ctx, trees, layout):
     H.assert_scores_close(step.scores, s, st, wl, name)
 
 
-def test_accumulate_over_layers_and_untouched_tail():
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_accumulate_over_layers_and_untouched_tail(layout):
+    """Layers after the first plan their work and fetch their first
+    context tile before the preceding kernel has finished."""
     wl = synth.tiny_workload(batch=2, layers=3)
-    st, inp, mode = H.build_case(wl, layers=3, ctx_lens=(150, 40),
+    st, inp, mode = H.build_case(wl, layers=3, ctx_lens=(150, 40), layout=layout,
                                  tree_sizes=(6, 3), seed=5)
-    step = H.make_step(wl, inp, mode)
+    step = H.make_step(wl, inp, mode, layout)
     step.scores.fill_(7.0)           # overwritten by layer 0, then summed
     step.run()
     torch.cuda.synchronize()
     total = 0
     for l in range(3):
-        o, s, _ = H.oracle_layer(wl, st, inp, l, "NHD", step.max_chunks)
+        o, s, _ = H.oracle_layer(wl, st, inp, l, layout, step.max_chunks)
         H.assert_attention_close(step.out[l], o, f"layer {l}")
         total = total + s
     H.assert_scores_close(step.scores, total, st, wl, "summed")
