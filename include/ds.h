@@ -320,16 +320,14 @@ ds_status ds_accept(const ds_accept_args* args, void* stream);
  * Refused with DS_ERR_UNSUPPORTED: args->n_nodes > DS_ACCEPT_STATIC_MAX_NODES
  * (use ds_accept).  Refused with DS_ERR_INVALID_ARG: a non-NULL workspace.
  *
- * Setup: the first call made while a given device is current looks up the
- * array's address on that device (cudaGetSymbolAddress) and keeps it for
- * the life of the process; make that first call before capturing `stream`
- * into a graph.  The kept address belongs to the device's context of that
- * time: after cudaDeviceReset (or any teardown of the primary context) the
- * array is reloaded elsewhere, so do not call ds_accept_static again in
- * that process.  Each call then enqueues, on
- * `stream`, a zeroing of the status word (the one part of the scratch that
- * must start at zero; the node records are written before they are read)
- * and the acceptance kernels.
+ * Every call looks up the array's address in the current context
+ * (cudaGetSymbolAddress, which allocates nothing), so a context torn down
+ * and created again (cudaDeviceReset) is followed correctly; make one call
+ * before capturing `stream` into a graph, so that the module is loaded
+ * outside the capture.  Each call then enqueues, on `stream`, a zeroing of
+ * the status word (the one part of the scratch that must start at zero;
+ * the node records are written before they are read) and the acceptance
+ * kernels.
  *
  * flags_out: NULL to return as soon as the work is enqueued; otherwise the
  * call synchronises `stream` and stores this call's device status bits

@@ -10,12 +10,11 @@
 // runs the same two kernels as ds_accept over it.
 //
 // Nothing here allocates: the array is part of the loaded module, its
-// address is looked up once per device, and each call only enqueues a
-// 256-byte memset of the status word and the acceptance kernels.
+// address is looked up on every call (the lookup allocates nothing), and
+// each call only enqueues a 256-byte memset of the status word and the
+// acceptance kernels.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "ds.h"
 #include "internal.h"
@@ -31,29 +30,16 @@ static_assert(kStaticBytes % kAlign == 0, "scratch must be a whole number of 256
 // same layout accept_layout() gives a caller's workspace
 static __device__ __align__(256) unsigned char g_accept_scratch[kStaticBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch[kMaxDevices] = {};
-
-// Address of g_accept_scratch on the current device, looked up on the first
-// call made with that device current.
+// Address of g_accept_scratch in the current context, looked up on every
+// call: the lookup allocates nothing, and a context that was torn down and
+// created again (cudaDeviceReset) never leaves a stale address behind.
 ds_status scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess)
-    return set_last_error(DS_ERR_CUDA, "ds_accept_static: cudaGetDevice failed");
-  if (dev < 0 || dev >= kMaxDevices)
-    return set_last_error(DS_ERR_UNSUPPORTED, "ds_accept_static: device ordinal >= 64");
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (e != cudaSuccess || !p)
-      return set_last_error(DS_ERR_CUDA,
-                            "ds_accept_static: cudaGetSymbolAddress of the scratch failed");
-    g_scratch[dev] = p;
-  }
-  *out = g_scratch[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+  if (e != cudaSuccess || !p)
+    return set_last_error(DS_ERR_CUDA,
+                          "ds_accept_static: cudaGetSymbolAddress of the scratch failed");
+  *out = p;
   return DS_OK;
 }
 
