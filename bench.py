@@ -338,9 +338,10 @@ OTHER_LAYERS = 4      # distinct layer caches per workload, rotated (> L2)
 def workload_block(name, dev, peak, reps=6):
     """Split pass, whole verify call, retrieval and acceptance of one of the
     other workloads: OTHER_LAYERS layers with their own caches are verified
-    back to back `reps` times; the split pass of every layer is bracketed by
-    CUDA events (per-call figures, so the dependent launch of the next call
-    is broken; the headline's own step is timed without that)."""
+    back to back `reps` times with the split pass of every layer bracketed
+    by CUDA events (the split-pass figure; the events break the dependent
+    launch of the next kernel), then `reps` times again with no event
+    between kernels (the verify-call figure)."""
     import torch
     from long_context_speculative_ds_gb300 import binding, synth
     from long_context_speculative_ds_gb300.step import StepInputs, VerifyStep
@@ -377,17 +378,24 @@ def workload_block(name, dev, peak, reps=6):
     for _ in range(3):
         step.run()
     torch.cuda.synchronize()
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    c0.record()
     for r in range(reps):
         for l in range(nl):
             binding.ds_verify_attn(pargs[r][l])
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    split_us = statistics.median(a.elapsed_time(b) * 1e3 for row in evs for a, b in row)
+    # whole verify calls back to back, with no event between their kernels
+    # (an event pair ends the dependent-launch overlap of the next kernel)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(reps):
+        for l in range(nl):
+            step.verify_layer(l)
     c1.record()
     torch.cuda.synchronize()
     assert step.device_status() == 0
     verify_us = c0.elapsed_time(c1) * 1e3 / (reps * nl)
-    split_us = statistics.median(a.elapsed_time(b) * 1e3 for row in evs for a, b in row)
 
     def alone(fn, n=10):
         fn()
