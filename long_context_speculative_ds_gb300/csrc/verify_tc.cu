@@ -11,7 +11,9 @@
 //               sequence end is copied with plain loads so that slots past
 //               the end read as zero, and pages wholly past the end get an
 //               out-of-range coordinate (TMA fills zeros).
-//   warp 1      tensor-memory allocator.
+//   warp 1      tensor-memory allocator; in the split that holds the tree's
+//               keys it then forms the tree's ancestor masks, beside the
+//               loader, for the softmax warps' tree units.
 //   warps 2, 3  MMA issuers of softmax groups 0 and 1 (one thread each).
 //   warps 4-7   softmax group 0, warps 8-11 softmax group 1 (each a whole
 //               warpgroup): one query row per thread, tensor-memory lane
