@@ -104,7 +104,12 @@ VerifyLayout verify_layout(const ds_verify_args& a, int num_sms) {
   L.group = a.num_q_heads / a.num_kv_heads;
   L.rg_max = (DS_MAX_TREE_NODES * L.group + kRowsPerItem - 1) / kRowsPerItem;
   L.target_ctas = num_sms;
-  L.max_items = num_sms + a.batch * a.num_kv_heads * L.rg_max;
+  // A batch of sequences of different lengths can round its splits badly in
+  // one wave of num_sms CTAs; the plan may then use two (see plan_refit), so
+  // the grid and the split outputs are sized for it.  A single sequence's
+  // row groups all have the same length and never need it.
+  L.wave_ctas = a.batch > 1 ? 2 * num_sms : 0;
+  L.max_items = (L.wave_ctas > 0 ? L.wave_ctas : num_sms) + a.batch * a.num_kv_heads * L.rg_max;
   size_t off = kStatusBytes;
   L.counters = off;
   off = align_up(off + (size_t)a.batch * a.num_kv_heads * L.rg_max * sizeof(uint32_t));

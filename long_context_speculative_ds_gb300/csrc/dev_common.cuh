@@ -38,6 +38,7 @@ struct PlanArgs {
   const int32_t* tree_offsets;
   int32_t batch, n_nodes, num_kv_heads, group, page_size, max_pages;
   int32_t chunk_size, max_chunks, target_ctas, rg_max;
+  int32_t wave_ctas;    // > target_ctas: items a two-wave plan may use (0: one wave only)
   uint32_t* status;
 };
 
@@ -130,6 +131,11 @@ static __device__ __noinline__ Plan plan_at(const PlanArgs& a, int b_sel, int it
 // target) tiles per split can need more items than there are CTAs, and the
 // extra items would run as a second wave.  When the plan p does, this takes
 // instead the smallest tiles-per-split whose items fit (when any does).
+// When that split is more than 15 % above the one-wave ideal (p.tps on
+// entry) and the grid has room for it (wave_ctas), the plan instead takes
+// the smallest tiles-per-split whose items fit in wave_ctas: about two
+// waves of half-size items, which the hardware hands to SMs as they free
+// up, so the rounding of each group's split count costs less.
 static __device__ __noinline__ Plan plan_refit(const PlanArgs& a, int b_sel, int item_sel,
                                                Plan p) {
   const int lane = threadIdx.x & 31;
@@ -156,10 +162,21 @@ static __device__ __noinline__ Plan plan_refit(const PlanArgs& a, int b_sel, int
   int32_t max_tiles, unused;
   items_for(p.tps, max_tiles);
   if (max_tiles <= p.tps || items_for(max_tiles, unused) > a.target_ctas) return p;
+  const int32_t ideal = p.tps;
   int32_t lo = p.tps, hi = max_tiles;   // items(lo) > target >= items(hi)
   while (hi - lo > 1) {
     const int32_t mid = lo + (hi - lo) / 2;
     if (items_for(mid, unused) <= a.target_ctas) hi = mid; else lo = mid;
+  }
+  if (a.wave_ctas > a.target_ctas && (int64_t)hi * 100 > (int64_t)ideal * 115) {
+    // items(lo2) > wave_ctas >= items(hi2); hi2 = hi fits, since the
+    // one-wave items do
+    int32_t lo2 = max(1, ideal / 2) - 1, hi2 = hi;
+    while (hi2 - lo2 > 1) {
+      const int32_t mid = lo2 + (hi2 - lo2) / 2;
+      if (items_for(mid, unused) <= a.wave_ctas) hi2 = mid; else lo2 = mid;
+    }
+    return plan_at(a, b_sel, item_sel, hi2);
   }
   return plan_at(a, b_sel, item_sel, hi);
 }

@@ -25,6 +25,7 @@ struct VerifyLayout {
   int32_t group;        // num_q_heads / num_kv_heads
   int32_t rg_max;       // row groups per (sequence, kv head) at 64 nodes
   int32_t target_ctas;  // CTAs the plan aims at
+  int32_t wave_ctas;    // items a two-wave plan may use (batches of more than one sequence; 0: none)
   int32_t max_items;    // upper bound on work items
   size_t counters;      // [batch][kv][rg_max] u32           splits finished (0 between calls)
   size_t gdesc;         // [batch][kv][rg_max] int4          first item and splits of the

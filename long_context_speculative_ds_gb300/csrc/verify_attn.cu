@@ -205,6 +205,7 @@ cudaError_t launch_verify(const ds_verify_args& a, const VerifyLayout& L,
   k.plan.chunk_size = a.chunk_size;
   k.plan.max_chunks = a.max_chunks;
   k.plan.target_ctas = L.target_ctas;
+  k.plan.wave_ctas = L.wave_ctas;
   k.plan.rg_max = L.rg_max;
   k.plan.status = reinterpret_cast<uint32_t*>(ws);
   k.num_q_heads = a.num_q_heads;
