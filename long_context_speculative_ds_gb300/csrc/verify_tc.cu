@@ -471,9 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per_h = sq.rg * sq.splits;
     kvh = local / per_h;
     rgi = (local % per_h) / sq.splits;
+    // The sequence's tiles in sq.splits near-equal ranges, the larger ones
+    // first (the last range holds the tree's tile): the split count comes
+    // from the plan's tiles per split, without full splits and a short
+    // remainder.
     const int split = local % sq.splits;
-    t0 = split * p.tps;
-    t1 = min(t0 + p.tps, sq.tiles);
+    const int base = sq.tiles / sq.splits, rem = sq.tiles % sq.splits;
+    t0 = split * base + min(split, rem);
+    t1 = t0 + base + (split < rem ? 1 : 0);
     rows_here = min(kRowsPerGroup, sq.rows - rgi * kRowsPerGroup);
   }
   const int nt = t1 - t0;
